@@ -1,0 +1,156 @@
+/*
+ * latent_tail.h - C ABI of the GB300 (sm_103a) latent-MoE output tail.
+ *
+ * The operation (Kimi-K3 latent MoE, as the vLLM PR #50383 and #51253 digests
+ * describe it):
+ *
+ *   x[t,l]   = sum_{p<P} routed[p,t,l]                      routed partial sum
+ *   y[t,l]   = x[t,l] * rsqrt(mean_l x[t,l]^2 + eps) * g[l]  RMSNorm with weight
+ *   out[t,h] = sum_l y[t,l] * W[h,l] + sum_{p<P} shared[p,t,h]
+ *
+ * Sources, by page and section:
+ *   - PR #51253 report, test source section: `_check_matches_replicated`
+ *     (expected = F.linear(F.rms_norm(all-reduced routed, (L,), g, EPS), W)
+ *     plus the all-reduced shared output) and `_check_writes_only_its_own_shard`
+ *     (a rank owning columns [start,end) adds latent . W[start:end]^T into only
+ *     those columns; the rest stays bit-identical).
+ *   - PR #50383 report, source of `_shard_up_proj_tail`: all-reduce then norm
+ *     (`allreduce_norm_latent_out`), `weight.narrow(0, start, size)` and
+ *     `shared_output.narrow(-1, start, size)`, then the beta-add epilogue
+ *     `hidden_shard.addmm_(latent, up_proj_shard.t())`.
+ *   On one GPU the P tensor-parallel partials are stacked tensors that the
+ *   kernels reduce; the column-parallel shard is the [col_start, col_end) option.
+ *
+ * Conventions for every entry point:
+ *   - bf16 tensors are passed as `uint16_t*` holding bfloat16 bit patterns.
+ *   - All arrays are DEVICE memory on the current CUDA device, contiguous and
+ *     row-major, allocated and owned by the caller. Every pointer must be
+ *     16-byte aligned. The library never allocates, frees or keeps a pointer
+ *     after the call returns.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream). No call synchronizes the host, except
+ *     latent_tail_check.
+ *   - Arguments are validated on the host before anything is enqueued. On a
+ *     non-OK status nothing was launched and no memory was touched.
+ *   - T == 0 is a no-op that returns LT_OK.
+ *   - Shape limits: 1 <= P <= 64; 8 <= L <= 16384 and L % 8 == 0;
+ *     8 <= H <= 1048576 and H % 8 == 0; 0 <= T <= 2^24. Violations give
+ *     LT_ERR_INVALID_ARG (range) or LT_ERR_ALIGNMENT (multiple of 8).
+ *   - Device-side waits are bounded: a wait that expires sets a device error
+ *     word and the kernel returns early; latent_tail_check reports it as
+ *     LT_ERR_TIMEOUT.
+ */
+#ifndef LATENT_TAIL_H
+#define LATENT_TAIL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define LT_API __attribute__((visibility("default")))
+#else
+#define LT_API
+#endif
+
+typedef enum lt_status {
+  LT_OK = 0,
+  LT_ERR_INVALID_ARG = 1, /* null pointer, bad shape/range, overlap, bad eps */
+  LT_ERR_ALIGNMENT = 2,   /* pointer not 16-byte aligned, or L/H/range not % 8 */
+  LT_ERR_UNSUPPORTED = 3, /* current device is not compute capability 10.3 */
+  LT_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
+  LT_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  LT_ERR_TIMEOUT = 6      /* a bounded device-side wait expired */
+} lt_status;
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* lt_stream;
+
+/*
+ * Bytes of device workspace latent_tail_forward / _forward_cols need for T
+ * tokens of latent width L: the normalized latent y [T, L] in bf16, rounded up
+ * to 256 bytes. P and H do not change it. Returns 0 for T <= 0 or invalid
+ * shapes. Host-only, never touches the GPU.
+ */
+LT_API size_t latent_tail_workspace_size(int P, int T, int L, int H);
+
+/*
+ * Whole tail for all H output columns (equivalent to latent_tail_forward_cols
+ * with col_start = 0, col_end = H).
+ *   routed      [P, T, L] bf16  routed-expert latent partials
+ *   shared      [P, T, H] bf16  shared-expert output partials
+ *   norm_weight [L]       fp32  RMSNorm weight g
+ *   W           [H, L]    bf16  up-projection weight (row h = output column h)
+ *   out         [T, H]    bf16  result, round-to-nearest-even; must not overlap
+ *                               any input or the workspace
+ *   eps                         RMSNorm epsilon, finite and > 0
+ *   workspace, workspace_bytes  at least latent_tail_workspace_size(P,T,L,H)
+ *                               bytes of device scratch; its contents on entry
+ *                               are ignored and on return are unspecified
+ * Launches two kernels: reduce + RMSNorm into the workspace, then the
+ * up-projection with the shared-partial epilogue (decode kernel for T <= 128,
+ * persistent tensor-core kernel above), chained by programmatic dependent
+ * launch. Capturable in a CUDA graph.
+ */
+LT_API lt_status latent_tail_forward(const uint16_t* routed, const uint16_t* shared,
+                                     const float* norm_weight, const uint16_t* W,
+                                     uint16_t* out, int P, int T, int L, int H,
+                                     float eps, void* workspace, size_t workspace_bytes,
+                                     lt_stream stream);
+
+/*
+ * Column-parallel form: writes only out[t, h] for col_start <= h < col_end.
+ * Every other byte of out (still the full [T, H] buffer) is left untouched.
+ * 0 <= col_start < col_end <= H, both multiples of 8. Each written element is
+ * computed exactly as latent_tail_forward computes it, so a set of calls whose
+ * ranges tile [0, H) reproduces the full call bit for bit.
+ */
+LT_API lt_status latent_tail_forward_cols(const uint16_t* routed, const uint16_t* shared,
+                                          const float* norm_weight, const uint16_t* W,
+                                          uint16_t* out, int P, int T, int L, int H,
+                                          float eps, int col_start, int col_end,
+                                          void* workspace, size_t workspace_bytes,
+                                          lt_stream stream);
+
+/*
+ * Steps 1-2 alone (the pages' `allreduce_norm_latent_out`): latent[t,l] =
+ * bf16_rn(x[t,l] * rsqrt(mean_l x^2 + eps) * g[l]) with x = sum_p routed[p,t,l]
+ * accumulated in FP32.
+ *   routed [P, T, L] bf16, norm_weight [L] fp32, latent [T, L] bf16 (output,
+ *   must not overlap the inputs).
+ */
+LT_API lt_status latent_tail_norm(const uint16_t* routed, const float* norm_weight,
+                                  uint16_t* latent, int P, int T, int L, float eps,
+                                  lt_stream stream);
+
+/*
+ * Steps 3-5 alone (the pages' narrowed `addmm_` beta-add plus the shared-partial
+ * sum): out[t,h] = bf16_rn(sum_l latent[t,l] * W[h,l] + sum_p shared[p,t,h]) for
+ * col_start <= h < col_end; other columns untouched.
+ *   latent [T, L] bf16, shared [P, T, H] bf16, W [H, L] bf16, out [T, H] bf16.
+ * Range rules as in latent_tail_forward_cols. With P = 1 this is the
+ * per-rank compute after the reference's all-reduce.
+ */
+LT_API lt_status latent_tail_project_cols(const uint16_t* latent, const uint16_t* shared,
+                                          const uint16_t* W, uint16_t* out, int P, int T,
+                                          int L, int H, int col_start, int col_end,
+                                          lt_stream stream);
+
+/*
+ * Synchronizes `stream`, then reports (and clears) the current device's error
+ * word: LT_ERR_TIMEOUT if a bounded device wait expired since the last check,
+ * LT_ERR_CUDA if the stream reported an error, LT_OK otherwise.
+ */
+LT_API lt_status latent_tail_check(lt_stream stream);
+
+/* Static, human-readable name of a status code. Never NULL. */
+LT_API const char* latent_tail_status_string(lt_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LATENT_TAIL_H */
