@@ -1,0 +1,398 @@
+"""Benchmark of the latent-MoE output tail on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|prefill|stress|tiny|decode_T1|...]
+
+A step is one call of the whole tail (routed reduce + RMSNorm, up-projection,
+shared-partial epilogue) on one batch of synthetic inputs. The default workload
+is the decode configuration (P=8, T=16, L=2048, H=7168). Inputs rotate over
+enough seeded sets that their total exceeds twice the L2 size, so every step
+streams W and the partials from HBM. Steps are replayed from CUDA graphs and
+timed with CUDA events on the launching stream, between a barrier and a device
+synchronize on both sides; with N > 1 each rank runs its own replica (token
+batches are independent, no collective) and the max time over ranks is used.
+
+Prints one JSON line. `--impl reference` times the CPU oracle instead (the
+only other code path this file may run), on a bounded sample of the same
+workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_BYTES = 126 * 1024 * 1024  # replaced by the device's value at run time
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps (capped)")
+    return ap.parse_args()
+
+
+def workload(name):
+    from latent_moe_output_gb300 import inputs
+
+    if name not in inputs.WORKLOADS:
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(inputs.WORKLOADS)}")
+    return inputs.WORKLOADS[name]
+
+
+def call_bytes(P, T, L, width):
+    """Algorithmic bytes of one call: routed + shared columns + W rows + out + g."""
+    return P * T * L * 2 + P * T * width * 2 + width * L * 2 + T * width * 2 + L * 4
+
+
+def project_bytes(P, T, L, width):
+    """Algorithmic bytes of the up-projection kernel alone: latent y + shared
+    columns + W rows + out."""
+    return T * L * 2 + P * T * width * 2 + width * L * 2 + T * width * 2
+
+
+def flops(T, L, width):
+    return 2 * T * width * L
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(
+            d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(w, budget_s=12.0, max_tokens=None):
+    """The oracle as it stands, single-threaded, on a bounded sample of tokens
+    of the same workload (drawn on the CPU with the workload's seed)."""
+    import numpy as np
+
+    import oracle
+    from latent_moe_output_gb300 import inputs
+
+    lib = oracle.load()
+    tokens = w.T if max_tokens is None else min(w.T, max_tokens)
+    x = inputs.make(w.P, tokens, w.L, w.H, w.seed, device="cpu", outliers=w.outlier_rows)
+    done, t0 = 0, time.perf_counter()
+    # one token first to size the sample
+    oracle.forward(x.routed[:, :1], x.shared[:, :1], x.g, x.W, x.eps, lib=lib)
+    per_tok = time.perf_counter() - t0
+    n = int(max(1, min(tokens, budget_s / max(per_tok, 1e-9))))
+    t0 = time.perf_counter()
+    oracle.forward(x.routed[:, :n], x.shared[:, :n], x.g, x.W, x.eps, lib=lib)
+    dt = time.perf_counter() - t0
+    done = n
+    return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {w.T} tokens of the {w.name} workload (P={w.P}, L={w.L}, "
+                      f"H={w.H}), FP32 single-threaded, {dt:.2f} s",
+            "host_cores": os.cpu_count()}
+
+
+def reference_arm(args):
+    """CPU oracle as the reference arm: K timed steps, each a bounded token sample."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from latent_moe_output_gb300 import inputs
+
+    w = workload(args.workload)
+    lib = oracle.load()
+    steps = max(1, args.steps)
+    total = steps + max(0, args.warmup)
+    x1 = inputs.make(w.P, 1, w.L, w.H, w.seed, device="cpu", outliers=w.outlier_rows)
+    t0 = time.perf_counter()
+    oracle.forward(x1.routed, x1.shared, x1.g, x1.W, x1.eps, lib=lib)
+    per_tok = time.perf_counter() - t0
+    per_step_budget = 120.0 / total
+    n = int(max(1, min(w.T, per_step_budget / max(per_tok, 1e-9))))
+    x = inputs.make(w.P, n, w.L, w.H, w.seed, device="cpu", outliers=w.outlier_rows)
+    for _ in range(max(0, args.warmup)):
+        oracle.forward(x.routed, x.shared, x.g, x.W, x.eps, lib=lib)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.forward(x.routed, x.shared, x.g, x.W, x.eps, lib=lib)
+    dt = time.perf_counter() - t0
+    value = n * steps / dt
+    line = {
+        "impl": "reference", "metric": "latent-tail tokens/s", "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "P": w.P, "T": w.T, "L": w.L, "H": w.H,
+                   "sample_tokens_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle", "cores": 1,
+                         "sample": f"{n} of {w.T} tokens per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def ours(args):
+    import torch
+
+    from latent_moe_output_gb300 import binding, inputs
+
+    rank, world, local = dist_setup(args.gpus)
+    w = workload(args.workload)
+    P, T, L, H = w.P, w.T, w.L, w.H
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", L2_BYTES) or L2_BYTES
+    lib = binding.load_library()
+
+    set_bytes = call_bytes(P, T, L, H) + T * L * 2
+    n_sets = max(2, -(-2 * l2 // set_bytes) + 1)
+    sets = []
+    for r in range(n_sets):
+        x = inputs.make(P, T, L, H, w.seed + 7919 * r + 104729 * rank, device=dev,
+                        outliers=w.outlier_rows)
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(binding.latent_tail_workspace_size(P, T, L, H), dtype=torch.uint8,
+                         device=dev)
+        sets.append((x, out, ws))
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        x, out, ws = sets[i % n_sets]
+        binding.latent_tail_forward(x.routed, x.shared, x.g, x.W, out, x.eps, ws, stream)
+
+    def project_only(i):
+        x, out, ws = sets[i % n_sets]
+        y = ws[:T * L * 2].view(torch.bfloat16).view(T, L)
+        binding.latent_tail_project_cols(y, x.shared, x.W, out, 0, H, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            step(i)
+    binding.latent_tail_check(stream)
+
+    chunk = min(args.steps, 50 * n_sets)
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    fn(i)
+        return g
+
+    def timed(fn, steps):
+        graphs = {}
+        plan = []
+        left = steps
+        while left > 0:
+            n = min(chunk, left)
+            if n not in graphs:
+                graphs[n] = capture(fn, n)
+            plan.append(graphs[n])
+            left -= n
+        for g in graphs.values():  # untimed replay: settle clocks and caches
+            g.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for g in plan:
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return e0.elapsed_time(e1) / 1e3  # seconds
+
+    with ClockSampler(local) as clocks:
+        t_step = timed(step, args.steps)
+    binding.latent_tail_check(stream)
+    t_step = max_over_ranks(t_step, world)
+    t_proj = max_over_ranks(timed(project_only, args.steps), world)
+    binding.latent_tail_check(stream)
+
+    # end to end: pinned host partials -> device -> tail -> host result, every step
+    e2e_steps = args.e2e_steps or min(args.steps, 500)
+    hx = sets[0][0]
+    h_routed = hx.routed.cpu().pin_memory()
+    h_shared = hx.shared.cpu().pin_memory()
+    h_out = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    d = {"routed": torch.empty_like(hx.routed), "shared": torch.empty_like(hx.shared),
+         "out": torch.empty(T, H, dtype=torch.bfloat16, device=dev),
+         "workspace": sets[0][2]}
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            binding.forward_host(h_routed, h_shared, hx.g, hx.W, hx.eps, h_out, d, stream)
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            binding.forward_host(h_routed, h_shared, hx.g, hx.W, hx.eps, h_out, d, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    binding.latent_tail_check(stream)
+
+    if rank != 0:
+        return
+    hbm, tc_burst, tc_sus, peak_kind = peaks()
+    tokens_per_s = T * args.steps * world / t_step
+    us_call = t_step / args.steps * 1e6
+    us_proj = t_proj / args.steps * 1e6
+    pb = project_bytes(P, T, L, H)
+    cb = call_bytes(P, T, L, H)
+    fl = flops(T, L, H)
+    proj_gbs = pb / (us_proj * 1e-6) / 1e9
+    call_gbs = cb / (us_call * 1e-6) / 1e9
+    bound = "hbm"
+    roof = {"kernel": "decode_kernel" if T <= 128 else "prefill_kernel", "bound": bound,
+            "achieved": round(proj_gbs, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(proj_gbs / hbm, 4), "traffic": None,
+            "algorithmic_bytes_per_launch": pb, "us_per_launch": round(us_proj, 3),
+            "peak_source": peak_kind}
+    call_roof = {"achieved": round(call_gbs, 1), "peak": hbm, "unit": "GB/s",
+                 "frac": round(call_gbs / hbm, 4), "algorithmic_bytes_per_call": cb,
+                 "tensor_tflops": round(fl / (us_call * 1e-6) / 1e12, 2),
+                 "tensor_frac_of_burst_peak": round(fl / (us_call * 1e-6) / 1e12 / tc_burst, 4)}
+    line = {
+        "metric": "latent-tail tokens/s", "value": round(tokens_per_s, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_step / args.steps * 1e3, 6), "us_per_call": round(us_call, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "P": P, "T": T, "L": L, "H": H, "eps": inputs.EPS,
+                   "parallelism": f"replicas{world}",
+                   "l2": f"inputs rotate over {n_sets} sets, {n_sets * set_bytes / 2**20:.0f} MiB"
+                         f" > 2x L2 ({l2 / 2**20:.0f} MiB)",
+                   "timing": "CUDA graphs of up to %d calls, CUDA events on the launching stream"
+                             % chunk},
+        "roofline": roof, "call_roofline": call_roof,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(T * e2e_steps * world / t_e2e, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": P * T * L * 2 + P * T * H * 2,
+                "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps},
+    }
+    if not args.no_cpu_baseline and world >= 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,58 @@
+// Library-internal host interface between the C-ABI layer (api.cu) and the
+// kernel translation units. Not installed, not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace lt {
+
+// Device error word bits (set with atomicOr by kernels, read by latent_tail_check).
+constexpr uint32_t kErrWaitTimeout = 1u;
+
+// Largest token count the decode (split-K, swap-AB) kernel serves; above it
+// the persistent tensor-core kernel runs.
+constexpr int kDecodeMaxTokens = 128;
+
+// Encodes a 2-D bf16 row-major [rows, cols] tensor map with a (64 x box_rows)
+// box and 128-byte swizzle. Returns false if the driver rejects it.
+bool make_map_bf16_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                         uint32_t box_rows);
+
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int max_smem_optin;
+  uint32_t* err_word;  // device address of the error word
+};
+
+struct NormArgs {
+  const uint16_t* routed;  // [P,T,L]
+  const float* g;          // [L]
+  uint16_t* y;             // [T,L]
+  int P, T, L;
+  float eps;
+};
+
+struct ProjectArgs {
+  const uint16_t* y;       // [T,L]
+  const uint16_t* shared;  // [P,T,H]
+  const uint16_t* W;       // [H,L]
+  uint16_t* out;           // [T,H]
+  int P, T, L, H;
+  int col_start, col_end;
+  bool pdl;                // launched right after the norm kernel, may overlap it
+};
+
+cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const DeviceInfo& dev,
+                        cudaStream_t stream);
+cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+// One-time per-device function attributes (dynamic shared memory limits).
+cudaError_t setup_norm(const DeviceInfo& dev);
+cudaError_t setup_decode(const DeviceInfo& dev);
+cudaError_t setup_prefill(const DeviceInfo& dev);
+
+}  // namespace lt

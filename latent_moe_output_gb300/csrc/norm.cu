@@ -1,0 +1,111 @@
+// Steps 1-2 of the latent-MoE tail: sum the P routed partials of each token in
+// FP32 and apply RMSNorm with weight g, writing the bf16 latent y[T,L].
+//
+// Follows `allreduce_norm_latent_out` in PR #50383's `_shard_up_proj_tail`
+// (all-reduce first, then the norm) and F.rms_norm as the PR #51253 test
+// calls it: y = x * rsqrt(mean(x^2) + eps) * g, mean over L.
+//
+// One CTA per token row: 256 threads each own 8-element (16-byte) chunks of
+// the row, load all P partials of a chunk before accumulating (p ascending),
+// keep x in shared memory, reduce the sum of squares with warp shuffles and
+// then write y = (x * r) * g rounded to bf16. Memory-bound: P*L*2 bytes in,
+// L*2 bytes out per token, every load a 16-byte vector.
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace lt {
+namespace {
+
+constexpr int kNormThreads = 256;
+constexpr int kMaxL = 16384;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void add8(float (&a)[8], const uint4& v) {
+  a[0] += bf16_lo(v.x);
+  a[1] += bf16_hi(v.x);
+  a[2] += bf16_lo(v.y);
+  a[3] += bf16_hi(v.y);
+  a[4] += bf16_lo(v.z);
+  a[5] += bf16_hi(v.z);
+  a[6] += bf16_lo(v.w);
+  a[7] += bf16_hi(v.w);
+}
+
+__global__ void __launch_bounds__(kNormThreads)
+    norm_kernel(const uint16_t* __restrict__ routed, const float* __restrict__ g,
+                uint16_t* __restrict__ y, int P, int T, int L, float eps, int trigger) {
+  extern __shared__ float4 xs4[];  // the token's x[L] in FP32
+  __shared__ float red[kNormThreads / 32];
+  if (trigger) pdl_launch_dependents();
+
+  const int t = blockIdx.x;
+  const int nchunk = L >> 3;
+  const size_t row_stride = static_cast<size_t>(T) * L;
+  const uint16_t* base = routed + static_cast<size_t>(t) * L;
+
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < nchunk; c += kNormThreads) {
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const uint16_t* src = base + static_cast<size_t>(c) * 8;
+    int p = 0;
+    for (; p + 8 <= P; p += 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = ld_stream_v4(src + (p + k) * row_stride);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) add8(a, v[k]);
+    }
+    for (; p < P; ++p) add8(a, ld_stream_v4(src + p * row_stride));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss += a[j] * a[j];
+    xs4[2 * c] = make_float4(a[0], a[1], a[2], a[3]);
+    xs4[2 * c + 1] = make_float4(a[4], a[5], a[6], a[7]);
+  }
+
+  ss = warp_sum(ss);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  if (warp == 0) {
+    float v = lane < kNormThreads / 32 ? red[lane] : 0.f;
+    v = warp_sum(v);
+    if (lane == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float r = 1.0f / sqrtf(red[0] / static_cast<float>(L) + eps);
+
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  uint4* dst = reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * L);
+  for (int c = threadIdx.x; c < nchunk; c += kNormThreads) {
+    const float4 x0 = xs4[2 * c], x1 = xs4[2 * c + 1];
+    const float4 g0 = __ldg(g4 + 2 * c), g1 = __ldg(g4 + 2 * c + 1);
+    uint4 o;
+    o.x = pack_bf16x2(x0.x * r * g0.x, x0.y * r * g0.y);
+    o.y = pack_bf16x2(x0.z * r * g0.z, x0.w * r * g0.w);
+    o.z = pack_bf16x2(x1.x * r * g1.x, x1.y * r * g1.y);
+    o.w = pack_bf16x2(x1.z * r * g1.z, x1.w * r * g1.w);
+    dst[c] = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t setup_norm(const DeviceInfo&) {
+  return cudaFuncSetAttribute(norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kMaxL * static_cast<int>(sizeof(float)));
+}
+
+cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const DeviceInfo&,
+                        cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(a.L) * sizeof(float);
+  norm_kernel<<<a.T, kNormThreads, smem, stream>>>(a.routed, a.g, a.y, a.P, a.T, a.L, a.eps,
+                                                   trigger_dependents ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace lt

@@ -1,0 +1,110 @@
+"""CUDA path versus the CPU oracle, element by element, at the pages' bf16
+tolerance (atol 8e-2, rtol 3e-2). Every config of the benchmark list plus
+ragged shapes that span several tiles and leave partial tails."""
+
+import numpy as np
+import pytest
+import torch
+
+from latent_moe_output_gb300 import binding, inputs
+
+import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    return gh.library()
+
+
+def check_full(x, c0=0, c1=None, what=""):
+    xd = gh.to_dev(x)
+    got = gh.run(xd, c0, c1)
+    H = x.W.shape[0]
+    c1 = H if c1 is None else c1
+    want = gh.oracle_rows(x, range(x.routed.shape[1]), c0, c1)
+    gh.assert_parity(got[:, c0:c1], want, what)
+    return got
+
+
+def test_tiny():
+    check_full(inputs.make_workload(inputs.TINY), what="tiny")
+
+
+def test_decode():
+    check_full(inputs.make_workload(inputs.DECODE), what="decode P8 T16")
+
+
+@pytest.mark.parametrize("w", inputs.DECODE_SWEEP, ids=lambda w: w.name)
+def test_decode_sweep(w):
+    check_full(inputs.make_workload(w), what=w.name)
+
+
+@pytest.mark.parametrize("P,T,L,H", [
+    (1, 1, 64, 128),       # single token, single partial, one tile
+    (3, 7, 328, 1000),     # ragged K-block (328 = 5*64 + 8) and ragged 128-row tile
+    (5, 17, 2048, 520),    # tokens not a multiple of 16
+    (2, 128, 512, 384),    # largest decode token count
+    (3, 129, 328, 1000),   # smallest prefill token count, ragged everywhere
+    (2, 300, 192, 776),    # several 128-token tiles plus a tail; ragged 256-col tile
+    (4, 520, 2048, 512),   # several token tiles at the production latent width
+    (1, 1000, 64, 2056),   # many tiles, one K-block, P = 1 (pre-reduced latent)
+    (16, 200, 256, 264),   # P = 16 partials
+])
+def test_ragged_shapes(P, T, L, H):
+    x = inputs.make(P, T, L, H, seed=P * 1000 + T)
+    check_full(x, what=f"P{P} T{T} L{L} H{H}")
+
+
+@pytest.mark.parametrize("w", [inputs.PREFILL, inputs.STRESS], ids=lambda w: w.name)
+def test_full_size_sampled_rows(w):
+    """Full BASELINE sizes on the device; the oracle checks every column of a
+    sample of token rows: first and last rows, rows around tile edges, the
+    outlier rows of the stress workload, and random rows."""
+    x = inputs.make_workload(w, device="cuda")
+    got = gh.run(x)
+    T = w.T
+    gen = np.random.default_rng(w.seed)
+    rows = {0, 1, 127, 128, 255, 256, T // 2, T - 129, T - 128, T - 2, T - 1}
+    rows |= set(gen.choice(T, 8, replace=False).tolist())
+    if w.outlier_rows:
+        rows |= set(x.scaled_up[:4].tolist()) | set(x.scaled_down[:4].tolist())
+    rows = sorted(rows)
+    want = gh.oracle_rows(x, rows)
+    gh.assert_parity(got[torch.as_tensor(rows, device=got.device)], want, w.name)
+    assert torch.isfinite(got.float()).all()
+
+
+def test_norm_stage_matches_oracle_latent():
+    import oracle
+
+    x = inputs.make(8, 37, 2048, 128, seed=9)
+    xd = gh.to_dev(x)
+    y = torch.empty(37, 2048, dtype=torch.bfloat16, device="cuda")
+    binding.latent_tail_norm(xd.routed, xd.g, y, x.eps)
+    binding.latent_tail_check()
+    want = oracle.latent(x.routed, x.g, x.eps)
+    # one bf16 rounding of an FP32 value: relative error <= 2^-8
+    err = np.abs(y.float().cpu().numpy() - want)
+    assert np.all(err <= 2.0 ** -8 * np.abs(want) + 1e-6)
+
+
+@pytest.mark.parametrize("T", [16, 600])
+def test_forward_equals_norm_then_project(T):
+    x = gh.to_dev(inputs.make(8, T, 2048, 1024, seed=T))
+    full = gh.run(x)
+    y = torch.empty(T, 2048, dtype=torch.bfloat16, device="cuda")
+    binding.latent_tail_norm(x.routed, x.g, y, x.eps)
+    out = torch.empty_like(full)
+    binding.latent_tail_project_cols(y, x.shared, x.W, out, 0, 1024)
+    binding.latent_tail_check()
+    assert torch.equal(out, full)
+
+
+def test_zero_tokens():
+    x = gh.to_dev(inputs.make(2, 0, 64, 128, seed=0))
+    out = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    binding.latent_tail_forward(x.routed, x.shared, x.g, x.W, out, x.eps, ws)
+    binding.latent_tail_check()
