@@ -37,11 +37,12 @@ L2_BYTES = 126 * 1024 * 1024  # replaced by the device's value at run time
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--T", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps (capped)")
     return ap.parse_args()
 
@@ -95,7 +96,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -239,6 +240,10 @@ def ours(args):
 
     rank, world, local = dist_setup(args.gpus)
     w = workload(args.workload)
+    if args.T:
+        import dataclasses
+
+        w = dataclasses.replace(w, name=f"{w.name}_T{args.T}", T=args.T)
     P, T, L, H = w.P, w.T, w.L, w.H
     dev = torch.device("cuda", local)
     props = torch.cuda.get_device_properties(dev)
@@ -291,24 +296,34 @@ def ours(args):
                 graphs[n] = capture(fn, n)
             plan.append(graphs[n])
             left -= n
-        for g in graphs.values():  # untimed replay: settle clocks and caches
-            g.replay()
-        stream.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for g in plan:
-            g.replay()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(world)
+        # CUDAGraph.replay() launches on the current stream: make it `stream`,
+        # the stream the events are recorded on.
+        with torch.cuda.stream(stream):
+            for g in graphs.values():  # untimed replay: settle clocks and caches
+                g.replay()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            barrier(world)
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            for g in plan:
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            barrier(world)
         return e0.elapsed_time(e1) / 1e3  # seconds
 
+    for _, out, _ in sets:  # poison outputs: the timed steps must overwrite them
+        out.fill_(float("nan"))
+    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
         t_step = timed(step, args.steps)
     binding.latent_tail_check(stream)
+    written = min(args.steps, n_sets)
+    for _, out, _ in sets[:written]:
+        if not torch.isfinite(out.float()).all():
+            raise RuntimeError("timed steps did not write their outputs")
     t_step = max_over_ranks(t_step, world)
     t_proj = max_over_ranks(timed(project_only, args.steps), world)
     binding.latent_tail_check(stream)

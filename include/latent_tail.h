@@ -146,6 +146,16 @@ LT_API lt_status latent_tail_project_cols(const uint16_t* latent, const uint16_t
  */
 LT_API lt_status latent_tail_check(lt_stream stream);
 
+/*
+ * Diagnostic for the bounded device waits: enqueues one CTA that waits on a
+ * barrier nothing ever completes, through the same bounded wait the kernels
+ * use, with a limit of limit_us microseconds (1 .. 1000000). The wait expires,
+ * the device error word records a timeout and the kernel returns; the next
+ * latent_tail_check on the stream reports LT_ERR_TIMEOUT and clears it. No
+ * fault, trap or hang is involved and the context stays usable.
+ */
+LT_API lt_status latent_tail_selftest_wait_timeout(unsigned int limit_us, lt_stream stream);
+
 /* Static, human-readable name of a status code. Never NULL. */
 LT_API const char* latent_tail_status_string(lt_status status);
 

@@ -52,6 +52,7 @@ _SIGNATURES = {
     "latent_tail_project_cols": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 6
                                  + [ctypes.c_void_p]),
     "latent_tail_check": (ctypes.c_int, [ctypes.c_void_p]),
+    "latent_tail_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint, ctypes.c_void_p]),
     "latent_tail_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 

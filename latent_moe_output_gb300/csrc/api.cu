@@ -251,6 +251,15 @@ LT_API lt_status latent_tail_check(lt_stream stream) {
   return LT_OK;
 }
 
+LT_API lt_status latent_tail_selftest_wait_timeout(unsigned int limit_us, lt_stream stream) {
+  if (limit_us < 1 || limit_us > 1000000) return LT_ERR_INVALID_ARG;
+  const lt::DeviceInfo* dev = nullptr;
+  lt_status st = current_device(&dev);
+  if (st != LT_OK) return st;
+  return launch_status(lt::launch_wait_probe(static_cast<uint64_t>(limit_us) * 1000u, *dev,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 LT_API const char* latent_tail_status_string(lt_status status) {
   switch (status) {
     case LT_OK: return "LT_OK: success";

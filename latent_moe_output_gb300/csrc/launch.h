@@ -50,6 +50,9 @@ cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const Device
 cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
+// One CTA waiting on a barrier nothing arrives at, bounded by limit_ns.
+cudaError_t launch_wait_probe(uint64_t limit_ns, const DeviceInfo& dev, cudaStream_t stream);
+
 // One-time per-device function attributes (dynamic shared memory limits).
 cudaError_t setup_norm(const DeviceInfo& dev);
 cudaError_t setup_decode(const DeviceInfo& dev);

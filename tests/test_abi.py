@@ -149,3 +149,8 @@ def test_norm_and_project_validation(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(FileNotFoundError):
         binding.load_library(tmp_path / "missing.so")
+
+
+def test_selftest_limit_validation(lib):
+    assert lib.latent_tail_selftest_wait_timeout(0, None) == Status.INVALID_ARG
+    assert lib.latent_tail_selftest_wait_timeout(1000001, None) == Status.INVALID_ARG
