@@ -156,6 +156,36 @@ LT_API lt_status latent_tail_check(lt_stream stream);
  */
 LT_API lt_status latent_tail_selftest_wait_timeout(unsigned int limit_us, lt_stream stream);
 
+/*
+ * Allocation-free form of latent_tail_forward (the pages have no counterpart;
+ * this exists for callers, not for the method). Some callers cannot allocate
+ * device memory: a custom op or plugin that a host runtime hands only its
+ * input and output buffers, with no allocator to call, or code that must not
+ * allocate while it runs. They cannot supply the workspace that
+ * latent_tail_forward needs, so this entry point keeps that scratch (the
+ * normalized latent, T * L * 2 bytes) in a fixed device array inside the
+ * library instead:
+ *   - the array holds LT_NOALLOC_MAX_SCRATCH_BYTES (1 MiB) on every GPU that
+ *     loads the library, until the process exits; calls with
+ *     T * L * 2 > LT_NOALLOC_MAX_SCRATCH_BYTES return LT_ERR_WORKSPACE and
+ *     launch nothing (at L = 2048 that allows T <= 256);
+ *   - nothing is allocated or freed by the call (no cudaMalloc / cudaFree);
+ *   - the first call on a device looks up the array's device address on that
+ *     device; make that first call before capturing a stream into a graph;
+ *   - all calls on a device share the one array and it keeps the previous
+ *     call's contents (every call overwrites all T * L * 2 bytes it reads, so
+ *     nothing needs to start at zero). Calls whose GPU work overlaps in time
+ *     (different streams without ordering, or different host threads) race on
+ *     the array and give wrong results: order them on one stream.
+ * Arguments, output and errors are as for latent_tail_forward, minus the
+ * workspace.
+ */
+#define LT_NOALLOC_MAX_SCRATCH_BYTES ((size_t)1 << 20)
+LT_API lt_status latent_tail_forward_noalloc(const uint16_t* routed, const uint16_t* shared,
+                                             const float* norm_weight, const uint16_t* W,
+                                             uint16_t* out, int P, int T, int L, int H,
+                                             float eps, lt_stream stream);
+
 /* Static, human-readable name of a status code. Never NULL. */
 LT_API const char* latent_tail_status_string(lt_status status);
 

@@ -53,6 +53,8 @@ _SIGNATURES = {
                                  + [ctypes.c_void_p]),
     "latent_tail_check": (ctypes.c_int, [ctypes.c_void_p]),
     "latent_tail_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint, ctypes.c_void_p]),
+    "latent_tail_forward_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4
+                                    + [ctypes.c_float, ctypes.c_void_p]),
     "latent_tail_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -181,6 +183,29 @@ def latent_tail_project_cols(latent, shared, W, out, col_start: int, col_end: in
     _check(load_library().latent_tail_project_cols(y, s, w, o, P, T, L, H, int(col_start),
                                                    int(col_end), _stream_handle(stream)),
            "latent_tail_project_cols")
+
+
+def latent_tail_forward_noalloc(routed, shared, norm_weight, W, out, eps: float,
+                                stream=None) -> None:
+    """Whole tail with the library's fixed 1 MiB device scratch instead of a
+    caller workspace (for callers that cannot allocate); T * L * 2 must fit."""
+    import torch
+
+    bf = torch.bfloat16
+    r = _dev(routed, "routed", bf, 3)
+    s = _dev(shared, "shared", bf, 3)
+    g = _dev(norm_weight, "norm_weight", torch.float32, 1)
+    w = _dev(W, "W", bf, 2)
+    o = _dev(out, "out", bf, 2)
+    P, T, L = routed.shape
+    H = W.shape[0]
+    if tuple(shared.shape) != (P, T, H) or tuple(W.shape) != (H, L) \
+            or tuple(out.shape) != (T, H) or tuple(norm_weight.shape) != (L,):
+        raise ValueError("inconsistent shapes: routed [P,T,L], shared [P,T,H], W [H,L], "
+                         "out [T,H], norm_weight [L]")
+    _check(load_library().latent_tail_forward_noalloc(r, s, g, w, o, P, T, L, H, float(eps),
+                                                      _stream_handle(stream)),
+           "latent_tail_forward_noalloc")
 
 
 def latent_tail_check(stream=None) -> None:
