@@ -250,7 +250,7 @@ def ours(args):
     l2 = getattr(props, "L2_cache_size", L2_BYTES) or L2_BYTES
     lib = binding.load_library()
 
-    set_bytes = call_bytes(P, T, L, H) + T * L * 2
+    set_bytes = call_bytes(P, T, L, H) + binding.latent_tail_workspace_size(P, T, L, H)
     n_sets = max(2, -(-2 * l2 // set_bytes) + 1)
     sets = []
     for r in range(n_sets):

@@ -131,8 +131,9 @@ LT_API lt_status latent_tail_norm(const uint16_t* routed, const float* norm_weig
  * sum): out[t,h] = bf16_rn(sum_l latent[t,l] * W[h,l] + sum_p shared[p,t,h]) for
  * col_start <= h < col_end; other columns untouched.
  *   latent [T, L] bf16, shared [P, T, H] bf16, W [H, L] bf16, out [T, H] bf16.
- * Range rules as in latent_tail_forward_cols. With P = 1 this is the
- * per-rank compute after the reference's all-reduce.
+ * Range rules as in latent_tail_forward_cols; results are bit-identical to the
+ * projection step of latent_tail_forward given the same latent. With P = 1 this
+ * is the per-rank compute after the reference's all-reduce.
  */
 LT_API lt_status latent_tail_project_cols(const uint16_t* latent, const uint16_t* shared,
                                           const uint16_t* W, uint16_t* out, int P, int T,
@@ -165,22 +166,23 @@ LT_API lt_status latent_tail_selftest_wait_timeout(unsigned int limit_us, lt_str
  * latent_tail_forward needs, so this entry point keeps that scratch (the
  * normalized latent, T * L * 2 bytes) in a fixed device array inside the
  * library instead:
- *   - the array holds LT_NOALLOC_MAX_SCRATCH_BYTES (1 MiB) on every GPU that
- *     loads the library, until the process exits; calls with
- *     T * L * 2 > LT_NOALLOC_MAX_SCRATCH_BYTES return LT_ERR_WORKSPACE and
- *     launch nothing (at L = 2048 that allows T <= 256);
+ *   - the array holds LT_NOALLOC_MAX_SCRATCH_BYTES (8 MiB) on every GPU that
+ *     loads the library, until the process exits; calls whose
+ *     latent_tail_workspace_size(P, T, L, H) exceeds it return LT_ERR_WORKSPACE
+ *     and launch nothing (at L = 2048 that allows T <= 2048);
  *   - nothing is allocated or freed by the call (no cudaMalloc / cudaFree);
  *   - the first call on a device looks up the array's device address on that
  *     device; make that first call before capturing a stream into a graph;
  *   - all calls on a device share the one array and it keeps the previous
- *     call's contents (every call overwrites all T * L * 2 bytes it reads, so
- *     nothing needs to start at zero). Calls whose GPU work overlaps in time
+ *     call's contents (every call rewrites all of the latent it reads, so
+ *     nothing needs to start at zero).
+ *     Calls whose GPU work overlaps in time
  *     (different streams without ordering, or different host threads) race on
  *     the array and give wrong results: order them on one stream.
  * Arguments, output and errors are as for latent_tail_forward, minus the
  * workspace.
  */
-#define LT_NOALLOC_MAX_SCRATCH_BYTES ((size_t)1 << 20)
+#define LT_NOALLOC_MAX_SCRATCH_BYTES ((size_t)8 << 20)
 LT_API lt_status latent_tail_forward_noalloc(const uint16_t* routed, const uint16_t* shared,
                                              const float* norm_weight, const uint16_t* W,
                                              uint16_t* out, int P, int T, int L, int H,

@@ -187,7 +187,7 @@ def latent_tail_project_cols(latent, shared, W, out, col_start: int, col_end: in
 
 def latent_tail_forward_noalloc(routed, shared, norm_weight, W, out, eps: float,
                                 stream=None) -> None:
-    """Whole tail with the library's fixed 1 MiB device scratch instead of a
+    """Whole tail with the library's fixed 8 MiB device scratch instead of a
     caller workspace (for callers that cannot allocate); T * L * 2 must fit."""
     import torch
 

@@ -133,7 +133,7 @@ lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const flo
   if (ws == nullptr || ws_bytes < need) return LT_ERR_WORKSPACE;
   if (!aligned16(ws)) return LT_ERR_ALIGNMENT;
   const Span so = span(out, static_cast<size_t>(T) * H * 2);
-  const Span sw = span(ws, latent_bytes(T, L));
+  const Span sw = span(ws, need);
   const Span inputs[] = {span(routed, static_cast<size_t>(P) * T * L * 2),
                          span(shared, static_cast<size_t>(P) * T * H * 2),
                          span(g, static_cast<size_t>(L) * 4),

@@ -6,19 +6,23 @@
 //
 // At these sizes the call is bound by streaming W (H*L*2 bytes) from HBM once,
 // so the kernel is shaped around that stream:
-//   * swap-AB tensor-core product: the MMA's M=128 rows are W rows (output
+//   * swap-AB tensor-core product: the MMA's M = 128 rows are W rows (output
 //     columns h), its N are the T tokens padded to a multiple of 16, K = L;
 //     the FP32 accumulator D[h][t] lives in TMEM;
-//   * one CTA per (128-row tile, K slice). The KS slices of a tile form one
-//     thread-block cluster; the KS partial accumulators are summed through
-//     distributed shared memory in a fixed order (q = 0..KS-1), so results do
-//     not depend on the requested column range;
-//   * W and y K-blocks (64 wide, 128-byte rows) arrive by TMA into a stage
-//     ring; one thread issues TMA, one issues tcgen05.mma; under programmatic
-//     dependent launch the W loads of the first stages are issued before
-//     waiting for the norm kernel that produces y;
-//   * epilogue: each CTA finishes 128/KS rows for all tokens, adding the P
-//     shared partials (p ascending) in FP32 and storing bf16.
+//   * one CTA per (128-row tile, K slice); the KS slices of a tile form one
+//     thread-block cluster. KS = 4 (two CTAs per SM) while its buffers fit in
+//     half an SM, else 2. Clusters of 8 cannot all be resident at once, which
+//     is why the split stops at 4;
+//   * W boxes (128 x 64, 128-byte swizzle) are requested before the rest of the
+//     set-up, and under programmatic dependent launch before waiting for the
+//     norm kernel that writes y; one thread issues TMA, one issues tcgen05.mma;
+//   * while W streams in, the epilogue warps sum the P shared partials of the
+//     rows this CTA finishes (p ascending, FP32) into shared memory;
+//   * after the MMAs, every CTA pushes each accumulator row into the shared
+//     memory of the cluster CTA that finishes that row (DSMEM stores), one
+//     cluster barrier, then each CTA adds the KS partials in fixed slice order
+//     plus the shared sum and stores bf16. The summation order never depends
+//     on the requested column range.
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -27,12 +31,15 @@
 namespace lt {
 namespace {
 
-constexpr int kBlockM = 128;                           // W rows per tile
-constexpr int kBlockK = 64;                            // K per stage (128-byte rows)
-constexpr int kThreads = 128;
-constexpr int kMaxStages = 8;
+constexpr int kBlockM = 128;                              // W rows per tile
+constexpr int kBlockK = 64;                               // K per stage (128-byte rows)
+constexpr int kThreads = 192;                             // TMA, MMA, 4 epilogue warps
+constexpr int kEpiThreads = 128;
+constexpr int kMaxStages = 16;
 constexpr uint32_t kWStageBytes = kBlockM * kBlockK * 2;  // 16 KB
-constexpr int kSmemBudget = 72 * 1024;                  // keeps 3 CTAs per SM
+constexpr int kSmemLimit = 220 * 1024;                   // + static smem <= opt-in max
+constexpr int kSmemBudget = 210 * 1024;                   // one CTA per SM
+constexpr int kHalfSmBudget = 110 * 1024;                 // two CTAs per SM
 
 struct DecodeParams {
   const uint16_t* shared;
@@ -46,6 +53,8 @@ struct DecodeParams {
   int npad;        // MMA N: tokens rounded up to a multiple of 16
   int stages;
   int tmem_cols;
+  uint32_t ssum_offset;  // byte offsets (from the 1024-aligned base) of the
+  uint32_t slot_offset;  // shared-partial sums and of the received K-slice partials
   int pdl;
   uint32_t* err;
 };
@@ -57,6 +66,21 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+__device__ __forceinline__ void add8(float (&a)[8], const uint4& v) {
+  a[0] += bf16_lo(v.x);
+  a[1] += bf16_hi(v.x);
+  a[2] += bf16_lo(v.y);
+  a[3] += bf16_hi(v.y);
+  a[4] += bf16_lo(v.z);
+  a[5] += bf16_hi(v.z);
+  a[6] += bf16_lo(v.w);
+  a[7] += bf16_hi(v.w);
+}
+
+// Shared-memory layout from the 1024-aligned base:
+//   [0, ring)          stage ring: W box [128 x 64] then y box [npad x 64], 128B swizzle
+//   [ssum_offset, ..)  ssum[t][r]: sum_p shared[p, t, h0 + r0 + r] for this CTA's rows
+//   [slot_offset, ..)  slot[src][r][t]: K-slice partial of row r0 + r pushed by CTA src
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap w_map,
                   const __grid_constant__ CUtensorMap y_map, const DecodeParams p) {
@@ -69,14 +93,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();
+  // K slice of this CTA; equal to its rank in the cluster (grid x == cluster x).
+  const uint32_t rank = blockIdx.x;
   const int h0 = (p.tile0 + static_cast<int>(blockIdx.y)) * kBlockM;
   const int kb_begin = static_cast<int>(rank) * p.kb_per_cta;
   const int nkb = max(0, min(p.total_kb, kb_begin + p.kb_per_cta) - kb_begin);
   const uint32_t stage_bytes = kWStageBytes + static_cast<uint32_t>(p.npad) * 128u;
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
-  float* part = reinterpret_cast<float*>(smem_raw + (sbase - raw_u32));  // [npad][128]
+  uint8_t* sgen = smem_raw + (sbase - raw_u32);
+  float* ssum = reinterpret_cast<float*>(sgen + p.ssum_offset);
+  float* slot = reinterpret_cast<float*>(sgen + p.slot_offset);
+  const int rpc = kBlockM / p.ks;  // output rows this CTA finishes
+  const int r0 = static_cast<int>(rank) * rpc;
+  const int groups = rpc / 8;      // 8-row (16-byte) groups per token
+  volatile int* abort_v = &abort_flag;
+  const int pre = min(p.stages, nkb);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -86,26 +118,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&acc_bar), 1);
     abort_flag = 0;
     mbar_fence_init();
-    tma_prefetch_map(&w_map);
-    tma_prefetch_map(&y_map);
+    // W does not depend on the preceding kernel: request the first stages now,
+    // before the rest of the set-up, so the HBM stream starts at once.
+    for (int i = 0; i < pre; ++i) {
+      const uint32_t fb = smem_u32(&full_bar[i]);
+      mbar_arrive_expect_tx(fb, stage_bytes);
+      tma_load_2d(sbase + static_cast<uint32_t>(i) * stage_bytes, &w_map, fb,
+                  (kb_begin + i) * kBlockK, h0);
+    }
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), static_cast<uint32_t>(p.tmem_cols));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  volatile int* abort_v = &abort_flag;
+  const bool have_acc = nkb > 0;
 
   if (warp == 0) {
     if (lane == 0 && nkb > 0) {
       // ---------------- TMA producer ----------------
-      const int pre = min(p.stages, nkb);
-      for (int i = 0; i < pre; ++i) {
-        const uint32_t st = sbase + static_cast<uint32_t>(i) * stage_bytes;
-        const uint32_t fb = smem_u32(&full_bar[i]);
-        mbar_arrive_expect_tx(fb, stage_bytes);
-        tma_load_2d(st, &w_map, fb, (kb_begin + i) * kBlockK, h0);
-      }
       if (p.pdl) pdl_wait();  // y is written by the preceding norm kernel
       for (int i = 0; i < pre; ++i) {
         const uint32_t st = sbase + static_cast<uint32_t>(i) * stage_bytes;
@@ -150,22 +181,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(smem_u32(&acc_bar));  // fires once every issued MMA has completed
     }
     __syncwarp();
-  }
-
-  // ---------------- epilogue part 1: TMEM -> shared-memory partial ----------------
-  const bool have_acc = nkb > 0;
-  bool ok = true;
-  if (have_acc) {
-    ok = mbar_wait(smem_u32(&acc_bar), 0, p.err, abort_v);
-    tc_fence_after();
-  }
-  ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below needs a converged warp
-  {
-    const int row = warp * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    // (a) While W streams in: sum the P shared partials of this CTA's rows,
+    //     p ascending in FP32, into shared memory. Independent of the norm kernel.
+    const int et = threadIdx.x - 64;
+    const size_t plane = static_cast<size_t>(p.T) * p.H;
+    const int items = p.T * groups;
+    for (int i = et; i < items; i += kEpiThreads) {
+      const int t = i / groups;
+      const int g = i - t * groups;
+      const int h = h0 + r0 + g * 8;
+      float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (h >= p.col_start && h < p.col_end) {
+        const uint16_t* src = p.shared + static_cast<size_t>(t) * p.H + h;
+        int pp = 0;
+        for (; pp + 8 <= p.P; pp += 8) {
+          uint4 v[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) v[k] = ld_stream_v4(src + (pp + k) * plane);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) add8(a, v[k]);
+        }
+        for (; pp < p.P; ++pp) add8(a, ld_stream_v4(src + pp * plane));
+      }
+      float4* dst = reinterpret_cast<float4*>(ssum + t * rpc + g * 8);
+      dst[0] = make_float4(a[0], a[1], a[2], a[3]);
+      dst[1] = make_float4(a[4], a[5], a[6], a[7]);
+    }
+    // (b) Accumulator rows -> the shared memory of the CTA that finishes them
+    //     (distributed shared memory stores into its slot[rank]).
+    bool ok = true;
+    if (have_acc) {
+      ok = mbar_wait(smem_u32(&acc_bar), 0, p.err, abort_v);
+      tc_fence_after();
+    }
+    ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below needs a converged warp
+    if (lane == 0 && warp == 2) pdl_launch_dependents();  // the next call may start its prologue
+    const int q = warp & 3;            // TMEM lane quadrant of this warp
+    const int row = q * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const int owner = row / rpc;
+    const uint32_t dst_row = smem_u32(slot) +
+        static_cast<uint32_t>(((static_cast<int>(rank) * rpc + (row - owner * rpc)) * p.npad) * 4);
+    const uint32_t dsm = map_to_rank(dst_row, static_cast<uint32_t>(owner));
     for (int c = 0; c < p.npad; c += 16) {
       float v[16];
-      __syncwarp();  // tcgen05.ld needs the whole warp converged
+      __syncwarp();
       if (have_acc && ok) {
         tmem_ld16(tmem + lane_base + static_cast<uint32_t>(c), v);
       } else {
@@ -173,46 +235,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 16; ++j) v[j] = 0.f;
       }
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (c + j < p.T) part[(c + j) * kBlockM + row] = v[j];
+      for (int j = 0; j < 16; j += 4)
+        st_dsmem_f32x4(dsm + static_cast<uint32_t>((c + j) * 4), v[j], v[j + 1], v[j + 2],
+                       v[j + 3]);
     }
   }
   __syncwarp();
-  cluster_sync();  // every slice's partial is now visible to the cluster
+  cluster_sync();  // all K-slice partials of this CTA's rows have arrived
 
-  // ---------------- epilogue part 2: split-K sum + shared partials ----------------
+  // (c) Finish this CTA's rows: K-slice partials summed in fixed order
+  //     (slice 0..KS-1), plus the shared-partial sum, rounded to bf16.
   {
-    const int rpc = kBlockM / p.ks;  // rows finished by this CTA
-    const int r0 = static_cast<int>(rank) * rpc;
-    const int my_row = threadIdx.x % rpc;
-    const int ngroups = kThreads / rpc;
-    const int tg = threadIdx.x / rpc;
-    const int h = h0 + r0 + my_row;
-    const bool col_ok = h >= p.col_start && h < p.col_end;
-    const uint32_t part_u32 = smem_u32(part);
-    uint32_t peer[8];
+    const int items = p.T * groups;
+    for (int i = threadIdx.x; i < items; i += kThreads) {
+      const int t = i / groups;
+      const int g = i - t * groups;
+      const int h = h0 + r0 + g * 8;
+      if (h < p.col_start || h >= p.col_end) continue;
+      float acc[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) peer[q] = q < p.ks ? map_to_rank(part_u32, q) : 0u;
-    const size_t plane = static_cast<size_t>(p.T) * p.H;
-    for (int t = tg; t < p.T; t += ngroups) {
-      const uint32_t off = static_cast<uint32_t>((t * kBlockM + r0 + my_row) * 4);
-      float acc = 0.f;
+      for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+      for (int src = 0; src < p.ks; ++src) {
+        const float* sp = slot + (src * rpc + g * 8) * p.npad + t;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (q < p.ks) acc += ld_dsmem_f32(peer[q] + off);
-      if (col_ok) {
-        const unsigned short* src =
-            reinterpret_cast<const unsigned short*>(p.shared) + static_cast<size_t>(t) * p.H + h;
-        float s = 0.f;
-        for (int pp = 0; pp < p.P; ++pp)
-          s += __uint_as_float(static_cast<uint32_t>(__ldg(src + pp * plane)) << 16);
-        const __nv_bfloat16 o = __float2bfloat16_rn(acc + s);
-        p.out[static_cast<size_t>(t) * p.H + h] = *reinterpret_cast<const uint16_t*>(&o);
+        for (int j = 0; j < 8; ++j) acc[j] += sp[j * p.npad];
       }
+      const float4* sp = reinterpret_cast<const float4*>(ssum + t * rpc + g * 8);
+      const float4 s0 = sp[0], s1 = sp[1];
+      uint4 o;
+      o.x = pack_bf16x2(acc[0] + s0.x, acc[1] + s0.y);
+      o.y = pack_bf16x2(acc[2] + s0.z, acc[3] + s0.w);
+      o.z = pack_bf16x2(acc[4] + s1.x, acc[5] + s1.y);
+      o.w = pack_bf16x2(acc[6] + s1.z, acc[7] + s1.w);
+      *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * p.H + h) = o;
     }
   }
-  __syncwarp();
-  cluster_sync();  // peers have finished reading this CTA's partial
 
   tc_fence_before();
   __syncthreads();
@@ -244,7 +301,7 @@ int env_int(const char* name, int dflt) {
 
 cudaError_t setup_decode(const DeviceInfo&) {
   return cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              1024 + 64 * 1024 + kSmemBudget);
+                              kSmemLimit);
 }
 
 cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
@@ -259,22 +316,49 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
   p.col_end = a.col_end;
   p.total_kb = ceil_div(a.L, kBlockK);
   p.npad = ceil_div(std::max(a.T, 1), 16) * 16;
-  // K split: a fixed function of L (never of the column range), so that every
+  // K split: a fixed function of (T, L), never of the column range, so every
   // output element is summed in the same order whatever range is requested.
-  int ks = std::max(1, std::min(8, p.total_kb / 4));
-  while (ks & (ks - 1)) ks &= ks - 1;  // power of two: 128 rows split evenly
+  // Four slices (224 CTAs at H = 7168, two per SM) when their buffers fit in
+  // half an SM's shared memory, else two (112 CTAs, one per SM), else one.
+  const uint32_t stage_bytes = kWStageBytes + static_cast<uint32_t>(p.npad) * 128u;
+  // bytes of the shared-partial sums plus the received partials for `cand` slices
+  auto extra_bytes = [&](int cand) {
+    const int rpc = kBlockM / cand;
+    const size_t ss = (static_cast<size_t>(p.npad) * rpc * 4 + 1023) & ~size_t(1023);
+    const size_t sl = (static_cast<size_t>(cand) * rpc * p.npad * 4 + 1023) & ~size_t(1023);
+    return ss + sl;
+  };
+  int ks = 1;
+  int stages = 1;
+  for (int cand : {4, 2}) {
+    if (p.total_kb < 4 * cand) continue;  // at least 4 K-blocks per slice
+    const long budget = cand == 4 ? kHalfSmBudget : kSmemBudget;
+    long st = (budget - 1024 - static_cast<long>(extra_bytes(cand))) /
+              static_cast<long>(stage_bytes);
+    st = std::min<long>({st, ceil_div(p.total_kb, cand), kMaxStages});
+    if (st < (cand == 4 ? 3 : 2)) continue;
+    ks = cand;
+    stages = static_cast<int>(st);
+    break;
+  }
+  if (ks == 1) {
+    const long st = (kSmemBudget - 1024 - static_cast<long>(extra_bytes(1))) /
+                    static_cast<long>(stage_bytes);
+    stages = static_cast<int>(std::max<long>(1, std::min<long>({st, p.total_kb, kMaxStages})));
+  }
 #ifdef LT_TUNING
   ks = env_int("LT_DECODE_KS", ks);
+  stages = std::min(std::max(1, env_int("LT_DECODE_STAGES", stages)),
+                    std::min(kMaxStages, ceil_div(p.total_kb, ks)));
 #endif
+  const size_t ring = static_cast<size_t>(stages) * stage_bytes;
   p.ks = ks;
   p.kb_per_cta = ceil_div(p.total_kb, ks);
-  const uint32_t stage_bytes = kWStageBytes + static_cast<uint32_t>(p.npad) * 128u;
-  int stages = std::min(p.kb_per_cta, std::max(1, kSmemBudget / static_cast<int>(stage_bytes)));
-  stages = std::min(stages, kMaxStages);
-#ifdef LT_TUNING
-  stages = std::min(std::max(1, env_int("LT_DECODE_STAGES", stages)), kMaxStages);
-#endif
   p.stages = stages;
+  const int rpc = kBlockM / ks;
+  p.ssum_offset = static_cast<uint32_t>(ring);
+  p.slot_offset = static_cast<uint32_t>(
+      ring + ((static_cast<size_t>(p.npad) * rpc * 4 + 1023) & ~size_t(1023)));
   p.tmem_cols = next_pow2_at_least(p.npad, 32);
   p.pdl = a.pdl ? 1 : 0;
   p.err = dev.err_word;
@@ -282,8 +366,8 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
   const int tile_last = (a.col_end - 1) / kBlockM;
   p.tile0 = tile_first;
   const int ntiles = tile_last - tile_first + 1;
-  const size_t part_bytes = static_cast<size_t>(p.npad) * kBlockM * sizeof(float);
-  const size_t smem = 1024 + std::max(static_cast<size_t>(stages) * stage_bytes, part_bytes);
+  const size_t smem = 1024 + ring + extra_bytes(ks);
+  if (smem > static_cast<size_t>(kSmemLimit)) return cudaErrorInvalidConfiguration;
 
   CUtensorMap w_map, y_map;
   if (!make_map_bf16_sw128(&w_map, a.W, a.H, a.L, kBlockM)) return cudaErrorInvalidValue;

@@ -7,9 +7,9 @@
 // allowed or not wanted at call time. Such a caller cannot obtain the
 // workspace latent_tail_forward asks for.
 //
-// How: the normalized latent y[T, L] (the only scratch the path needs) lives
-// in the file-scope device array below. Every GPU that loads this library
-// holds it, 1 MiB, until the process exits. Host code must not pass the
+// How: the path's only scratch, the normalized latent y[T, L], lives in the
+// file-scope device array below. Every GPU that loads this library holds it, 8 MiB, until the
+// process exits. Host code must not pass the
 // array's name to a kernel (on the host it names a host-side shadow, not
 // device memory); its device address is looked up once per device with
 // cudaGetSymbolAddress and cached.
@@ -19,7 +19,7 @@
 
 #include <mutex>
 
-static constexpr size_t kStaticScratchBytes = LT_NOALLOC_MAX_SCRATCH_BYTES;  // T*L*2 at most
+static constexpr size_t kStaticScratchBytes = LT_NOALLOC_MAX_SCRATCH_BYTES;
 
 // The scratch itself: one per device, shared by every call on that device.
 static __device__ __align__(256) unsigned char g_static_latent[kStaticScratchBytes];
@@ -57,7 +57,7 @@ extern "C" LT_API lt_status latent_tail_forward_noalloc(const uint16_t* routed,
                                                         int T, int L, int H, float eps,
                                                         lt_stream stream) {
   const size_t need = latent_tail_workspace_size(P, T, L, H);
-  if (need > kStaticScratchBytes) return LT_ERR_WORKSPACE;  // T * L too large for the array
+  if (need > kStaticScratchBytes) return LT_ERR_WORKSPACE;  // too large for the array
   if (T <= 0 || need == 0)  // nothing to stage: let the regular entry point validate / no-op
     return latent_tail_forward(routed, shared, norm_weight, W, out, P, T, L, H, eps, nullptr, 0,
                                stream);

@@ -41,6 +41,10 @@ __global__ void __launch_bounds__(kNormThreads)
                 uint16_t* __restrict__ y, int P, int T, int L, float eps, int trigger) {
   extern __shared__ float4 xs4[];  // the token's x[L] in FP32
   __shared__ float red[kNormThreads / 32];
+  // Launched as a programmatic dependent of whatever precedes it on the stream:
+  // wait for that work (it may produce `routed` or still read the latent buffer)
+  // before touching memory, then let the projection kernel start its prologue.
+  pdl_wait();
   if (trigger) pdl_launch_dependents();
 
   const int t = blockIdx.x;
@@ -102,10 +106,18 @@ cudaError_t setup_norm(const DeviceInfo&) {
 
 cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const DeviceInfo&,
                         cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(a.L) * sizeof(float);
-  norm_kernel<<<a.T, kNormThreads, smem, stream>>>(a.routed, a.g, a.y, a.P, a.T, a.L, a.eps,
-                                                   trigger_dependents ? 1 : 0);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.T), 1, 1);
+  cfg.blockDim = dim3(kNormThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(a.L) * sizeof(float);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, norm_kernel, a.routed, a.g, a.y, a.P, a.T, a.L, a.eps,
+                            trigger_dependents ? 1 : 0);
 }
 
 }  // namespace lt

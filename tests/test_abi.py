@@ -67,6 +67,7 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     assert lib.latent_tail_workspace_size(8, 16, 2048, 7168) == 16 * 2048 * 2
+    assert lib.latent_tail_workspace_size(8, 8192, 2048, 7168) == 8192 * 2048 * 2
     assert lib.latent_tail_workspace_size(2, 5, 64, 128) == 768  # 640 rounded up to 256
     assert lib.latent_tail_workspace_size(8, 0, 2048, 7168) == 0
     assert lib.latent_tail_workspace_size(8, 16, 2047, 7168) == 0
@@ -138,12 +139,11 @@ def test_norm_and_project_validation(lib):
     assert lib.latent_tail_norm(A, C, E, 2, 4, 60, 1e-6, None) == Status.ALIGNMENT
     assert lib.latent_tail_norm(A, C, E, 2, 4, 64, 0.0, None) == Status.INVALID_ARG
     assert lib.latent_tail_norm(A, C, A + 16, 2, 4, 64, 1e-6, None) == Status.INVALID_ARG
-    assert lib.latent_tail_project_cols(A, B, D, E, 2, 4, 64, 128, 0, 136, None) == \
-        Status.INVALID_ARG
-    assert lib.latent_tail_project_cols(A, B, D, B + 32, 2, 4, 64, 128, 0, 128, None) == \
-        Status.INVALID_ARG
-    assert lib.latent_tail_project_cols(A, B, None, E, 2, 4, 64, 128, 0, 128, None) == \
-        Status.INVALID_ARG
+    pc = lib.latent_tail_project_cols
+    assert pc(A, B, D, E, 2, 4, 64, 128, 0, 136, None) == Status.INVALID_ARG
+    assert pc(A, B, D, B + 32, 2, 4, 64, 128, 0, 128, None) == Status.INVALID_ARG
+    assert pc(A, B, None, E, 2, 4, 64, 128, 0, 128, None) == Status.INVALID_ARG
+    assert pc(A, B, D, E + 8, 2, 4, 64, 128, 0, 128, None) == Status.ALIGNMENT
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

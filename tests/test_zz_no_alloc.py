@@ -2,8 +2,8 @@
 
 It serves callers that cannot allocate device memory (a custom op that its
 host runtime gives only input and output buffers, or code that must not
-allocate while it runs): the normalized-latent scratch lives in a fixed 1 MiB
-device array inside the library instead of a caller workspace. These tests
+allocate while it runs): the path's scratch lives in a fixed 8 MiB device
+array inside the library instead of a caller workspace. These tests
 call it through the C ABI and compare it with latent_tail_forward on two calls
 in a row, so the second call also shows that the first call's leftovers in the
 shared array do not leak into the result. The file sorts last so that a run
@@ -53,9 +53,9 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row():
 
 def test_noalloc_rejects_sizes_beyond_the_static_scratch():
     lib = gh.library()
-    # T * L * 2 = 257 * 2048 * 2 bytes > 1 MiB: rejected before any launch
-    x = gh.to_dev(inputs.make(1, 257, 2048, 128, seed=5))
-    out = torch.zeros(257, 128, dtype=torch.bfloat16, device="cuda")
+    # workspace 2049 * 2048 * 2 bytes > 8 MiB: rejected before any launch
+    x = gh.to_dev(inputs.make(1, 2049, 2048, 128, seed=5))
+    out = torch.zeros(2049, 128, dtype=torch.bfloat16, device="cuda")
     st = _noalloc(lib, x, out, torch.cuda.current_stream())
     assert st == Status.WORKSPACE
     binding.latent_tail_check()
