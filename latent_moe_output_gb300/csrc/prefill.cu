@@ -4,17 +4,26 @@
 // (`hidden_shard.addmm_(latent, up_proj_shard.t())`), with the shared-partial
 // sum of the final all-reduce done in the GEMM epilogue.
 //
-// Persistent, warp-specialized tcgen05 kernel, one CTA per SM:
-//   warp 0      TMA producer: y tile [128 tokens x 64] and W tile [256 rows x 64]
-//               per K-block into a 4-stage ring (128-byte swizzle);
+// At these sizes the dominant traffic is the P shared partials (P*T*H*2 bytes,
+// 69-74% of all bytes), so the kernel is built around two concurrent streams:
+// the tensor-core mainloop, fed from L2 (y and W are re-read per tile), and
+// the HBM stream of shared partials, fed by TMA independently of the MMAs.
+//
+// Persistent, warp-specialized tcgen05 kernel, one CTA per SM, 7 warps:
+//   warp 0      operand producer: y tile [128 tokens x 64] and W tile
+//               [256 rows x 64] per K-block into a 3-stage ring (128B swizzle,
+//               L2 evict-last: every operand tile is read by many CTAs);
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
-//               (M = 128 tokens, N = 256 output columns, K = 16 per instruction);
-//   warps 2..5  epilogue: TMEM -> registers (32 columns at a time), add the P
-//               shared partials with 16-byte loads, round to bf16, 16-byte stores.
-// Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile run
-// while the MMAs of the next tile accumulate. Output tiles sit at absolute
-// multiples of 256 columns, so a column-range call computes each element
-// exactly as the full call does.
+//               (M = 128 tokens, N = 256 output columns, K = 16 per instruction)
+//               into one of two TMEM accumulators (2 x 256 columns);
+//   warp 6      shared-partial producer: for every tile, 64-column chunk and
+//               partial p, one TMA box [128 tokens x 64 columns] into a 4-slot
+//               ring (L2 evict-first: read once);
+//   warps 2..5  epilogue, one token row per thread: sum the P partial boxes of
+//               a chunk in FP32 (p ascending), add the accumulator columns from
+//               TMEM, round to bf16 and store 16-byte vectors.
+// Output tiles sit at absolute multiples of 256 columns, so a column-range call
+// computes each element exactly as the full call does.
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -23,19 +32,23 @@
 namespace lt {
 namespace {
 
-constexpr int kTileT = 128;  // tokens per tile (MMA M)
-constexpr int kTileH = 256;  // output columns per tile (MMA N)
+constexpr int kTileT = 128;   // tokens per tile (MMA M)
+constexpr int kTileH = 256;   // output columns per tile (MMA N)
 constexpr int kBlockK = 64;
-constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kStages = 3;
+constexpr int kChunk = 64;    // output columns per shared-partial box
+constexpr int kChunks = kTileH / kChunk;
+constexpr int kSlots = 4;     // shared-partial ring depth
+constexpr int kThreads = 224;
 constexpr uint32_t kAStage = kTileT * kBlockK * 2;  // 16 KB of y
 constexpr uint32_t kBStage = kTileH * kBlockK * 2;  // 32 KB of W
 constexpr uint32_t kStageBytes = kAStage + kBStage;
+constexpr uint32_t kSlotBytes = kTileT * kChunk * 2;  // 16 KB
 constexpr uint32_t kTmemCols = 2 * kTileH;
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes;
+constexpr size_t kSmemBytes =
+    1024 + static_cast<size_t>(kStages) * kStageBytes + static_cast<size_t>(kSlots) * kSlotBytes;
 
 struct PrefillParams {
-  const uint16_t* shared;
   uint16_t* out;
   int P, T, L, H;
   int col_start, col_end;
@@ -65,7 +78,12 @@ __device__ __forceinline__ TileCoord tile_coord(const PrefillParams& p, int tile
   return c;
 }
 
-// Adds 8 bf16 values of one shared partial to s[0..7].
+// A 64-column chunk is processed only if it meets [col_start, col_end).
+__device__ __forceinline__ bool chunk_active(const PrefillParams& p, int hc) {
+  return hc < p.col_end && hc + kChunk > p.col_start;
+}
+
+// Adds the 8 bf16 values of a 16-byte word to s[0..7].
 __device__ __forceinline__ void add8(float* s, const uint4& v) {
   s[0] += bf16_lo(v.x);
   s[1] += bf16_hi(v.x);
@@ -79,18 +97,24 @@ __device__ __forceinline__ void add8(float* s, const uint4& v) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap y_map,
-                   const __grid_constant__ CUtensorMap w_map, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap w_map,
+                   const __grid_constant__ CUtensorMap s_map, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kStages];
   __shared__ uint64_t empty_bar[kStages];
   __shared__ uint64_t accf_bar[2];
   __shared__ uint64_t acce_bar[2];
+  __shared__ uint64_t sfull_bar[kSlots];
+  __shared__ uint64_t sempty_bar[kSlots];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
+  const uint32_t slot_base = sbase + kStages * kStageBytes;
+  const uint8_t* slot_gen = smem_raw + (slot_base - raw_u32);
   const int num_tiles = p.n_ttiles * p.n_htiles;
   const int my_tiles =
       static_cast<int>(blockIdx.x) < num_tiles
@@ -106,10 +130,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&accf_bar[a]), 1);
       mbar_init(smem_u32(&acce_bar[a]), 4 * 32);
     }
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(smem_u32(&sfull_bar[s]), 1);
+      mbar_init(smem_u32(&sempty_bar[s]), 4);  // one arrival per epilogue warp
+    }
     abort_flag = 0;
     mbar_fence_init();
     tma_prefetch_map(&y_map);
     tma_prefetch_map(&w_map);
+    tma_prefetch_map(&s_map);
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
   tc_fence_before();
@@ -120,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0 && my_tiles > 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- operand producer ----------------
+      const uint64_t keep = policy_evict_last();
       const int total = my_tiles * p.total_kb;
       const int pre = min(kStages, total);
       auto coord_of = [&](int it, TileCoord& c, int& kb) {
@@ -135,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = sbase + static_cast<uint32_t>(it) * kStageBytes;
         const uint32_t fb = smem_u32(&full_bar[it]);
         mbar_arrive_expect_tx(fb, kStageBytes);
-        tma_load_2d(st + kAStage, &w_map, fb, kb * kBlockK, c.h0);
+        tma_load_2d_hint(st + kAStage, &w_map, fb, kb * kBlockK, c.h0, keep);
       }
       if (p.pdl) pdl_wait();
       for (int it = 0; it < pre; ++it) {
@@ -143,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kb;
         coord_of(it, c, kb);
         const uint32_t st = sbase + static_cast<uint32_t>(it) * kStageBytes;
-        tma_load_2d(st, &y_map, smem_u32(&full_bar[it]), kb * kBlockK, c.t0);
+        tma_load_2d_hint(st, &y_map, smem_u32(&full_bar[it]), kb * kBlockK, c.t0, keep);
       }
       int issued = pre;
       for (int it = pre; it < total; ++it) {
@@ -156,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = sbase + static_cast<uint32_t>(s) * kStageBytes;
         const uint32_t fb = smem_u32(&full_bar[s]);
         mbar_arrive_expect_tx(fb, kStageBytes);
-        tma_load_2d(st, &y_map, fb, kb * kBlockK, c.t0);
-        tma_load_2d(st + kAStage, &w_map, fb, kb * kBlockK, c.h0);
+        tma_load_2d_hint(st, &y_map, fb, kb * kBlockK, c.t0, keep);
+        tma_load_2d_hint(st + kAStage, &w_map, fb, kb * kBlockK, c.h0, keep);
         issued = it + 1;
       }
       if (*abort_v) {
@@ -198,69 +228,114 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+  } else if (warp == 6) {
+    if (lane == 0 && my_tiles > 0) {
+      // ---------------- shared-partial producer ----------------
+      const uint64_t once = policy_evict_first();
+      int k = 0;
+      bool alive = true;
+      for (int i = 0; i < my_tiles && alive; ++i) {
+        const TileCoord c =
+            tile_coord(p, static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x));
+        for (int ch = 0; ch < kChunks && alive; ++ch) {
+          const int hc = c.h0 + ch * kChunk;
+          if (!chunk_active(p, hc)) continue;
+          for (int pp = 0; pp < p.P; ++pp, ++k) {
+            const int s = k % kSlots;
+            const uint32_t round = static_cast<uint32_t>(k / kSlots);
+            if (!mbar_wait(smem_u32(&sempty_bar[s]), (round & 1u) ^ 1u, p.err, abort_v)) {
+              alive = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(&sfull_bar[s]);
+            mbar_arrive_expect_tx(fb, kSlotBytes);
+            tma_load_2d_hint(slot_base + static_cast<uint32_t>(s) * kSlotBytes, &s_map, fb, hc,
+                             pp * p.T + c.t0, once);
+          }
+        }
+      }
+      if (*abort_v) {
+        for (int kk = max(0, k - kSlots); kk < k; ++kk)
+          wait_drain(smem_u32(&sfull_bar[kk % kSlots]), static_cast<uint32_t>(kk / kSlots) & 1u);
+      }
+    }
+    __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int q = warp & 3;       // TMEM lane quadrant this warp may access
+    const int r = q * 32 + lane;  // token row within the tile
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    const size_t plane = static_cast<size_t>(p.T) * p.H;
-    for (int i = 0; i < my_tiles; ++i) {
+    int k = 0;
+    bool alive = true;
+    for (int i = 0; i < my_tiles && alive; ++i) {
       const int acc = i & 1;
       const uint32_t use = static_cast<uint32_t>(i >> 1);
-      bool ok = mbar_wait(smem_u32(&accf_bar[acc]), use & 1u, p.err, abort_v);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
       const TileCoord c =
           tile_coord(p, static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x));
-      const int t = c.t0 + q * 32 + lane;
+      const int t = c.t0 + r;
       const bool row_ok = t < p.T;
       const uint32_t dcol = tmem + lane_base + static_cast<uint32_t>(acc * kTileH);
+      bool acc_ready = false;
 #pragma unroll 1
-      for (int ch = 0; ch < kTileH / 32; ++ch) {
-        const int hb = c.h0 + ch * 32;
-        float v[32];
+      for (int ch = 0; ch < kChunks; ++ch) {
+        const int hc = c.h0 + ch * kChunk;
+        const bool active = chunk_active(p, hc);
+        float s[kChunk];
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j) s[j] = 0.f;
+        if (active) {
+          // sum the P partial boxes of this chunk, p ascending
+          for (int pp = 0; pp < p.P; ++pp, ++k) {
+            const int sl = k % kSlots;
+            const uint32_t round = static_cast<uint32_t>(k / kSlots);
+            bool ok = mbar_wait(smem_u32(&sfull_bar[sl]), round & 1u, p.err, abort_v);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+              alive = false;
+              break;
+            }
+            const uint8_t* row_ptr = slot_gen + sl * kSlotBytes + r * 128;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {  // 16-byte chunk g of the row sits at g ^ (r % 8)
+              const uint4 v = *reinterpret_cast<const uint4*>(row_ptr + ((g ^ (r & 7)) << 4));
+              add8(&s[g * 8], v);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sempty_bar[sl]));
+          }
+          if (!alive) break;
+        }
+        if (!acc_ready) {
+          bool ok = mbar_wait(smem_u32(&accf_bar[acc]), use & 1u, p.err, abort_v);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) {
+            alive = false;
+            break;
+          }
+          tc_fence_after();
+          acc_ready = true;
+        }
+        float v0[32], v1[32];
         __syncwarp();  // tcgen05.ld needs the whole warp converged
-        tmem_ld32(dcol + static_cast<uint32_t>(ch * 32), v);
-        if (ch == kTileH / 32 - 1) {  // accumulator fully read: hand it back to the MMA warp
+        tmem_ld32(dcol + static_cast<uint32_t>(ch * kChunk), v0);
+        tmem_ld32(dcol + static_cast<uint32_t>(ch * kChunk + 32), v1);
+        if (ch == kChunks - 1) {  // accumulator fully read: hand it back to the MMA warp
           tc_fence_before();
           mbar_arrive(smem_u32(&acce_bar[acc]));
         }
-        if (!row_ok || hb >= p.col_end || hb + 32 <= p.col_start) continue;
-        bool gv[4];  // 8-column groups inside [col_start, col_end) (col_end <= H)
+        if (!active || !row_ok) continue;
+        uint16_t* dst = p.out + static_cast<size_t>(t) * p.H + hc;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) gv[g] = hb + g * 8 >= p.col_start && hb + g * 8 < p.col_end;
-        float s[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) s[j] = 0.f;
-        const uint16_t* src = p.shared + static_cast<size_t>(t) * p.H + hb;
-        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-        int pp = 0;
-        for (; pp + 4 <= p.P; pp += 4) {
-          uint4 w[4][4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-              w[k][g] = gv[g] ? ld_stream_v4(src + (pp + k) * plane + g * 8) : zero;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int g = 0; g < 4; ++g) add8(&s[g * 8], w[k][g]);
-        }
-        for (; pp < p.P; ++pp) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
-            add8(&s[g * 8], gv[g] ? ld_stream_v4(src + pp * plane + g * 8) : zero);
-        }
-        uint16_t* dst = p.out + static_cast<size_t>(t) * p.H + hb;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          if (!gv[g]) continue;
+        for (int g = 0; g < 8; ++g) {
+          const int hh = hc + g * 8;
+          if (hh < p.col_start || hh >= p.col_end) continue;
+          const float* a = g < 4 ? &v0[g * 8] : &v1[(g - 4) * 8];
+          const float* b = &s[g * 8];
           uint4 o;
-          o.x = pack_bf16x2(v[g * 8 + 0] + s[g * 8 + 0], v[g * 8 + 1] + s[g * 8 + 1]);
-          o.y = pack_bf16x2(v[g * 8 + 2] + s[g * 8 + 2], v[g * 8 + 3] + s[g * 8 + 3]);
-          o.z = pack_bf16x2(v[g * 8 + 4] + s[g * 8 + 4], v[g * 8 + 5] + s[g * 8 + 5]);
-          o.w = pack_bf16x2(v[g * 8 + 6] + s[g * 8 + 6], v[g * 8 + 7] + s[g * 8 + 7]);
+          o.x = pack_bf16x2(a[0] + b[0], a[1] + b[1]);
+          o.y = pack_bf16x2(a[2] + b[2], a[3] + b[3]);
+          o.z = pack_bf16x2(a[4] + b[4], a[5] + b[5]);
+          o.w = pack_bf16x2(a[6] + b[6], a[7] + b[7]);
           *reinterpret_cast<uint4*>(dst + g * 8) = o;
         }
       }
@@ -292,7 +367,6 @@ cudaError_t setup_prefill(const DeviceInfo&) {
 
 cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   PrefillParams p{};
-  p.shared = a.shared;
   p.out = a.out;
   p.P = a.P;
   p.T = a.T;
@@ -309,9 +383,15 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   const long long tiles = static_cast<long long>(p.n_htiles) * p.n_ttiles;
   const int grid = static_cast<int>(std::min<long long>(dev.num_sms, tiles));
 
-  CUtensorMap y_map, w_map;
+  // The shared partials as one 2-D tensor [P*T rows, H columns]: the box for
+  // (partial p, tokens t0..t0+127) starts at row p*T + t0. Rows past T inside
+  // a partial belong to the next partial and are never stored; rows past P*T
+  // and columns past H read as zero.
+  CUtensorMap y_map, w_map, s_map;
   if (!make_map_bf16_sw128(&y_map, a.y, a.T, a.L, kTileT)) return cudaErrorInvalidValue;
   if (!make_map_bf16_sw128(&w_map, a.W, a.H, a.L, kTileH)) return cudaErrorInvalidValue;
+  if (!make_map_bf16_sw128(&s_map, a.shared, static_cast<uint64_t>(a.P) * a.T, a.H, kTileT))
+    return cudaErrorInvalidValue;
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -327,7 +407,7 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   }
   cfg.attrs = attrs;
   cfg.numAttrs = static_cast<unsigned>(n);
-  return cudaLaunchKernelEx(&cfg, prefill_kernel, y_map, w_map, p);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel, y_map, w_map, s_map, p);
 }
 
 }  // namespace lt

@@ -109,6 +109,12 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // ------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with 128-byte swizzling: rows of 128 B (64 bf16 of K), 8-row atoms 1024 B
