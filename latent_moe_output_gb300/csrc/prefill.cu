@@ -35,18 +35,27 @@ namespace {
 constexpr int kTileT = 128;   // tokens per tile (MMA M)
 constexpr int kTileH = 256;   // output columns per tile (MMA N)
 constexpr int kBlockK = 64;
-constexpr int kStages = 3;
+constexpr int kMaxStages = 4;
 constexpr int kChunk = 64;    // output columns per shared-partial box
 constexpr int kChunks = kTileH / kChunk;
-constexpr int kSlots = 4;     // shared-partial ring depth
+constexpr int kMaxSlots = 8;  // shared-partial ring depth limit
 constexpr int kThreads = 224;
 constexpr uint32_t kAStage = kTileT * kBlockK * 2;  // 16 KB of y
 constexpr uint32_t kBStage = kTileH * kBlockK * 2;  // 32 KB of W
 constexpr uint32_t kStageBytes = kAStage + kBStage;
 constexpr uint32_t kSlotBytes = kTileT * kChunk * 2;  // 16 KB
 constexpr uint32_t kTmemCols = 2 * kTileH;
-constexpr size_t kSmemBytes =
-    1024 + static_cast<size_t>(kStages) * kStageBytes + static_cast<size_t>(kSlots) * kSlotBytes;
+constexpr size_t kSmemLimit = 226 * 1024;  // + static shared memory <= opt-in maximum
+
+// Shared memory splits between the operand ring (feeds the MMAs from L2) and
+// the shared-partial ring (feeds the epilogue from HBM); both hide latency,
+// so each gets as many bytes in flight as the other allows.
+constexpr int kDefaultStages = 3;
+constexpr int kDefaultSlots = 4;
+
+size_t smem_bytes(int stages, int slots) {
+  return 1024 + static_cast<size_t>(stages) * kStageBytes + static_cast<size_t>(slots) * kSlotBytes;
+}
 
 struct PrefillParams {
   uint16_t* out;
@@ -56,6 +65,8 @@ struct PrefillParams {
   int n_htiles;
   int n_ttiles;
   int total_kb;
+  int stages;       // operand ring depth
+  int slots;        // shared-partial ring depth
   int pdl;
   uint32_t* err;
 };
@@ -100,12 +111,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap w_map,
                    const __grid_constant__ CUtensorMap s_map, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[kStages];
-  __shared__ uint64_t empty_bar[kStages];
+  __shared__ uint64_t full_bar[kMaxStages];
+  __shared__ uint64_t empty_bar[kMaxStages];
   __shared__ uint64_t accf_bar[2];
   __shared__ uint64_t acce_bar[2];
-  __shared__ uint64_t sfull_bar[kSlots];
-  __shared__ uint64_t sempty_bar[kSlots];
+  __shared__ uint64_t sfull_bar[kMaxSlots];
+  __shared__ uint64_t sempty_bar[kMaxSlots];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -113,7 +124,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
-  const uint32_t slot_base = sbase + kStages * kStageBytes;
+  const int kStages = p.stages;
+  const int kSlots = p.slots;
+  const uint32_t slot_base = sbase + static_cast<uint32_t>(kStages) * kStageBytes;
   const uint8_t* slot_gen = smem_raw + (slot_base - raw_u32);
   const int num_tiles = p.n_ttiles * p.n_htiles;
   const int my_tiles =
@@ -358,11 +371,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+#ifdef LT_TUNING
+#include <cstdlib>
+int env_int(const char* name, int dflt) {
+  const char* s = std::getenv(name);
+  return s ? std::atoi(s) : dflt;
+}
+#endif
+
 }  // namespace
 
 cudaError_t setup_prefill(const DeviceInfo&) {
   return cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmemBytes));
+                              static_cast<int>(kSmemLimit));
 }
 
 cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
@@ -378,6 +399,14 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   p.n_htiles = (a.col_end - 1) / kTileH - p.htile0 + 1;
   p.n_ttiles = ceil_div(a.T, kTileT);
   p.total_kb = ceil_div(a.L, kBlockK);
+  p.stages = kDefaultStages;
+  p.slots = kDefaultSlots;
+#ifdef LT_TUNING
+  p.stages = std::min(std::max(1, env_int("LT_PREFILL_STAGES", p.stages)), kMaxStages);
+  p.slots = std::min(std::max(1, env_int("LT_PREFILL_SLOTS", p.slots)), kMaxSlots);
+#endif
+  const size_t smem = smem_bytes(p.stages, p.slots);
+  if (smem > kSmemLimit) return cudaErrorInvalidConfiguration;
   p.pdl = a.pdl ? 1 : 0;
   p.err = dev.err_word;
   const long long tiles = static_cast<long long>(p.n_htiles) * p.n_ttiles;
@@ -396,7 +425,7 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attrs[1];
   int n = 0;
