@@ -154,15 +154,21 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(v, world):
+def max_over_ranks(v, world, device="cuda"):
+    """Largest value over all ranks (the job's time is its slowest rank's)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(tokens_per_rank_step, steps, world, seconds):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank_step * steps * world / seconds
 
 
 def cpu_baseline(w, budget_s=12.0, max_tokens=None):
@@ -355,7 +361,7 @@ def ours(args):
     if rank != 0:
         return
     hbm, tc_burst, tc_sus, peak_kind = peaks()
-    tokens_per_s = T * args.steps * world / t_step
+    tokens_per_s = job_throughput(T, args.steps, world, t_step)
     us_call = t_step / args.steps * 1e6
     us_proj = t_proj / args.steps * 1e6
     pb = project_bytes(P, T, L, H)
@@ -388,7 +394,7 @@ def ours(args):
         "roofline": roof, "call_roofline": call_roof,
         "gpu_launches": 2 * args.steps,
         "clocks": clocks.summary(),
-        "e2e": {"value": round(T * e2e_steps * world / t_e2e, 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(T, e2e_steps, world, t_e2e), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": P * T * L * 2 + P * T * H * 2,
                 "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps},
     }
