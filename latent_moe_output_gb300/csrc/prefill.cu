@@ -9,19 +9,27 @@
 // the tensor-core mainloop, fed from L2 (y and W are re-read per tile), and
 // the HBM stream of shared partials, fed by TMA independently of the MMAs.
 //
-// Persistent, warp-specialized tcgen05 kernel, one CTA per SM, 7 warps:
-//   warp 0      operand producer: y tile [128 tokens x 64] and W tile
-//               [256 rows x 64] per K-block into a 3-stage ring (128B swizzle,
-//               L2 evict-last: every operand tile is read by many CTAs);
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
-//               (M = 128 tokens, N = 256 output columns, K = 16 per instruction)
-//               into one of two TMEM accumulators (2 x 256 columns);
+// Each SM can take in only about 120 GB/s from L2 through TMA, so the bytes a
+// CTA must ingest per tile bound the kernel. Pairs of CTAs (a 2-CTA cluster)
+// therefore share one tensor-core product (tcgen05 cta_group::2, M = 256
+// tokens, N = 256 columns): each CTA loads its own 128 tokens of y and half of
+// the W tile, which halves the operand bytes per CTA.
+//
+// Persistent, warp-specialized kernel, one CTA per SM, 7 warps per CTA:
+//   warp 0      operand producer: y [128 tokens x 64] and W [128 rows x 64] per
+//               K-block into this CTA's stage ring (128B swizzle, L2 evict-last:
+//               every operand tile is read by many CTAs);
+//   warp 1      TMEM allocation for the pair; in the even CTA the single-thread
+//               MMA issuer (both CTAs' TMA copies of a stage complete on the even
+//               CTA's barrier; its commits arrive on the stage and accumulator
+//               barriers of both CTAs);
 //   warp 6      shared-partial producer: for every tile, 64-column chunk and
-//               partial p, one TMA box [128 tokens x 64 columns] into a 4-slot
+//               partial p, one TMA box [128 tokens x 64 columns] into a slot
 //               ring (L2 evict-first: read once);
 //   warps 2..5  epilogue, one token row per thread: sum the P partial boxes of
 //               a chunk in FP32 (p ascending), add the accumulator columns from
-//               TMEM, round to bf16 and store 16-byte vectors.
+//               this CTA's TMEM (two 256-column accumulators), round to bf16 and
+//               store 16-byte vectors.
 // Output tiles sit at absolute multiples of 256 columns, so a column-range call
 // computes each element exactly as the full call does.
 #include "launch.h"
@@ -32,16 +40,17 @@
 namespace lt {
 namespace {
 
-constexpr int kTileT = 128;   // tokens per tile (MMA M)
+constexpr int kTileT = 128;   // tokens per CTA (half of the pair's MMA M = 256)
 constexpr int kTileH = 256;   // output columns per tile (MMA N)
+constexpr int kHalfH = kTileH / 2;  // W rows loaded by each CTA of the pair
 constexpr int kBlockK = 64;
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kChunk = 64;    // output columns per shared-partial box
 constexpr int kChunks = kTileH / kChunk;
 constexpr int kMaxSlots = 8;  // shared-partial ring depth limit
 constexpr int kThreads = 224;
 constexpr uint32_t kAStage = kTileT * kBlockK * 2;  // 16 KB of y
-constexpr uint32_t kBStage = kTileH * kBlockK * 2;  // 32 KB of W
+constexpr uint32_t kBStage = kHalfH * kBlockK * 2;  // 16 KB of W (this CTA's half)
 constexpr uint32_t kStageBytes = kAStage + kBStage;
 constexpr uint32_t kSlotBytes = kTileT * kChunk * 2;  // 16 KB
 constexpr uint32_t kTmemCols = 2 * kTileH;
@@ -50,8 +59,8 @@ constexpr size_t kSmemLimit = 226 * 1024;  // + static shared memory <= opt-in m
 // Shared memory splits between the operand ring (feeds the MMAs from L2) and
 // the shared-partial ring (feeds the epilogue from HBM); both hide latency,
 // so each gets as many bytes in flight as the other allows.
-constexpr int kDefaultStages = 3;
-constexpr int kDefaultSlots = 4;
+constexpr int kDefaultStages = 4;
+constexpr int kDefaultSlots = 5;
 
 size_t smem_bytes(int stages, int slots) {
   return 1024 + static_cast<size_t>(stages) * kStageBytes + static_cast<size_t>(slots) * kSlotBytes;
@@ -63,7 +72,7 @@ struct PrefillParams {
   int col_start, col_end;
   int htile0;       // absolute index of the first 256-column tile
   int n_htiles;
-  int n_ttiles;
+  int n_tpairs;     // 256-token groups (one per CTA pair and tile)
   int total_kb;
   int stages;       // operand ring depth
   int slots;        // shared-partial ring depth
@@ -79,12 +88,13 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
 }
 
 struct TileCoord {
-  int t0, h0;
+  int t0, h0;  // this CTA's first token and the tile's first output column
 };
 
-__device__ __forceinline__ TileCoord tile_coord(const PrefillParams& p, int tile) {
+// Pair tile `tile` -> coordinates for the CTA of rank `rank` in the pair.
+__device__ __forceinline__ TileCoord tile_coord(const PrefillParams& p, int tile, int rank) {
   TileCoord c;
-  c.t0 = (tile / p.n_htiles) * kTileT;
+  c.t0 = (tile / p.n_htiles) * (2 * kTileT) + rank * kTileT;
   c.h0 = (p.htile0 + tile % p.n_htiles) * kTileH;
   return c;
 }
@@ -111,10 +121,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap w_map,
                    const __grid_constant__ CUtensorMap s_map, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[kMaxStages];
-  __shared__ uint64_t empty_bar[kMaxStages];
-  __shared__ uint64_t accf_bar[2];
-  __shared__ uint64_t acce_bar[2];
+  __shared__ uint64_t full_bar[kMaxStages];   // even CTA: both CTAs' stage s landed
+  __shared__ uint64_t empty_bar[kMaxStages];  // stage consumed by the pair MMAs
+  __shared__ uint64_t accf_bar[2];            // accumulator ready (both CTAs)
+  __shared__ uint64_t acce_bar[2];            // even CTA: accumulator drained by both
   __shared__ uint64_t sfull_bar[kMaxSlots];
   __shared__ uint64_t sempty_bar[kMaxSlots];
   __shared__ uint32_t tmem_slot;
@@ -122,28 +132,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_rank());  // 0 issues the pair MMAs
+  const int pair = static_cast<int>(blockIdx.x) >> 1;
+  const int n_pairs = static_cast<int>(gridDim.x) >> 1;
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
-  const int kStages = p.stages;
-  const int kSlots = p.slots;
-  const uint32_t slot_base = sbase + static_cast<uint32_t>(kStages) * kStageBytes;
+  const int n_stages = p.stages;
+  const int n_slots = p.slots;
+  const uint32_t slot_base = sbase + static_cast<uint32_t>(n_stages) * kStageBytes;
   const uint8_t* slot_gen = smem_raw + (slot_base - raw_u32);
-  const int num_tiles = p.n_ttiles * p.n_htiles;
-  const int my_tiles =
-      static_cast<int>(blockIdx.x) < num_tiles
-          ? (num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-          : 0;
+  const int num_tiles = p.n_tpairs * p.n_htiles;
+  const int my_tiles = pair < num_tiles ? (num_tiles - 1 - pair) / n_pairs + 1 : 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < n_stages; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&accf_bar[a]), 1);
-      mbar_init(smem_u32(&acce_bar[a]), 4 * 32);
+      mbar_init(smem_u32(&acce_bar[a]), 2 * 4);  // one arrival per epilogue warp of the pair
     }
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < n_slots; ++s) {
       mbar_init(smem_u32(&sfull_bar[s]), 1);
       mbar_init(smem_u32(&sempty_bar[s]), 4);  // one arrival per epilogue warp
     }
@@ -153,32 +163,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&w_map);
     tma_prefetch_map(&s_map);
   }
-  if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+  if (warp == 1) tmem_alloc_pair(smem_u32(&tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_v = &abort_flag;
 
   if (warp == 0) {
     if (lane == 0 && my_tiles > 0) {
-      // ---------------- operand producer ----------------
+      // ---------------- operand producer (this CTA's halves) ----------------
+      // Both CTAs' loads of stage s complete on the even CTA's full_bar[s]; the
+      // even CTA expects the bytes of both.
       const uint64_t keep = policy_evict_last();
       const int total = my_tiles * p.total_kb;
-      const int pre = min(kStages, total);
+      const int pre = min(n_stages, total);
       auto coord_of = [&](int it, TileCoord& c, int& kb) {
         const int local = it / p.total_kb;
         kb = it - local * p.total_kb;
-        c = tile_coord(p, static_cast<int>(blockIdx.x) + local * static_cast<int>(gridDim.x));
+        c = tile_coord(p, pair + local * n_pairs, rank);
       };
+      auto full_of = [&](int s) { return map_to_rank(smem_u32(&full_bar[s]), 0); };
       for (int it = 0; it < pre; ++it) {  // W does not depend on the norm kernel
         TileCoord c;
         int kb;
         coord_of(it, c, kb);
         const uint32_t st = sbase + static_cast<uint32_t>(it) * kStageBytes;
-        const uint32_t fb = smem_u32(&full_bar[it]);
-        mbar_arrive_expect_tx(fb, kStageBytes);
-        tma_load_2d_hint(st + kAStage, &w_map, fb, kb * kBlockK, c.h0, keep);
+        if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[it]), 2 * kStageBytes);
+        tma_load_2d_pair_hint(st + kAStage, &w_map, full_of(it), kb * kBlockK,
+                              c.h0 + rank * kHalfH, keep);
       }
       if (p.pdl) pdl_wait();
       for (int it = 0; it < pre; ++it) {
@@ -186,58 +200,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kb;
         coord_of(it, c, kb);
         const uint32_t st = sbase + static_cast<uint32_t>(it) * kStageBytes;
-        tma_load_2d_hint(st, &y_map, smem_u32(&full_bar[it]), kb * kBlockK, c.t0, keep);
+        tma_load_2d_pair_hint(st, &y_map, full_of(it), kb * kBlockK, c.t0, keep);
       }
       int issued = pre;
       for (int it = pre; it < total; ++it) {
-        const int s = it % kStages;
-        const uint32_t round = static_cast<uint32_t>(it / kStages);
-        if (!mbar_wait(smem_u32(&empty_bar[s]), (round & 1u) ^ 1u, p.err, abort_v)) break;
+        const int s = it % n_stages;
+        const uint32_t round = static_cast<uint32_t>(it / n_stages);
+        if (!mbar_wait_cluster(smem_u32(&empty_bar[s]), (round & 1u) ^ 1u, p.err, abort_v)) break;
         TileCoord c;
         int kb;
         coord_of(it, c, kb);
         const uint32_t st = sbase + static_cast<uint32_t>(s) * kStageBytes;
-        const uint32_t fb = smem_u32(&full_bar[s]);
-        mbar_arrive_expect_tx(fb, kStageBytes);
-        tma_load_2d_hint(st, &y_map, fb, kb * kBlockK, c.t0, keep);
-        tma_load_2d_hint(st + kAStage, &w_map, fb, kb * kBlockK, c.h0, keep);
+        if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * kStageBytes);
+        tma_load_2d_pair_hint(st, &y_map, full_of(s), kb * kBlockK, c.t0, keep);
+        tma_load_2d_pair_hint(st + kAStage, &w_map, full_of(s), kb * kBlockK, c.h0 + rank * kHalfH,
+                              keep);
         issued = it + 1;
       }
-      if (*abort_v) {
-        for (int it = max(0, issued - kStages); it < issued; ++it)
-          wait_drain(smem_u32(&full_bar[it % kStages]), static_cast<uint32_t>(it / kStages) & 1u);
+      if (*abort_v && rank == 0) {  // the even CTA's barriers count both CTAs' copies
+        for (int it = max(0, issued - n_stages); it < issued; ++it)
+          wait_drain(smem_u32(&full_bar[it % n_stages]), static_cast<uint32_t>(it / n_stages) & 1u);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && my_tiles > 0) {
-      // ---------------- MMA issuer ----------------
-      const uint32_t idesc = umma_idesc_bf16(kTileT, kTileH);
-      int it = 0;
-      bool alive = true;
-      for (int i = 0; i < my_tiles && alive; ++i) {
-        const int acc = i & 1;
-        const uint32_t use = static_cast<uint32_t>(i >> 1);
-        if (!mbar_wait(smem_u32(&acce_bar[acc]), (use & 1u) ^ 1u, p.err, abort_v)) break;
-        tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>(acc * kTileH);
-        for (int kb = 0; kb < p.total_kb; ++kb, ++it) {
-          const int s = it % kStages;
-          const uint32_t round = static_cast<uint32_t>(it / kStages);
-          if (!mbar_wait(smem_u32(&full_bar[s]), round & 1u, p.err, abort_v)) {
-            alive = false;
-            break;
-          }
+      if (rank == 0) {
+        // ---------------- pair MMA issuer ----------------
+        const uint32_t idesc = umma_idesc_bf16(2 * kTileT, kTileH);
+        int it = 0;
+        bool alive = true;
+        for (int i = 0; i < my_tiles && alive; ++i) {
+          const int acc = i & 1;
+          const uint32_t use = static_cast<uint32_t>(i >> 1);
+          if (!mbar_wait_cluster(smem_u32(&acce_bar[acc]), (use & 1u) ^ 1u, p.err, abort_v)) break;
           tc_fence_after();
-          const uint32_t a = sbase + static_cast<uint32_t>(s) * kStageBytes;
-          const uint32_t b = a + kAStage;
+          const uint32_t d = tmem + static_cast<uint32_t>(acc * kTileH);
+          for (int kb = 0; kb < p.total_kb; ++kb, ++it) {
+            const int s = it % n_stages;
+            const uint32_t round = static_cast<uint32_t>(it / n_stages);
+            if (!mbar_wait_cluster(smem_u32(&full_bar[s]), round & 1u, p.err, abort_v)) {
+              alive = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a = sbase + static_cast<uint32_t>(s) * kStageBytes;
+            const uint32_t b = a + kAStage;
 #pragma unroll
-          for (int k = 0; k < kBlockK / 16; ++k)
-            umma_bf16(d, umma_desc_sw128(a + 32u * k), umma_desc_sw128(b + 32u * k), idesc,
-                      (kb | k) != 0 ? 1u : 0u);
-          umma_commit(smem_u32(&empty_bar[s]));
+            for (int k = 0; k < kBlockK / 16; ++k)
+              umma_bf16_pair(d, umma_desc_sw128(a + 32u * k), umma_desc_sw128(b + 32u * k), idesc,
+                             (kb | k) != 0 ? 1u : 0u);
+            umma_commit_pair(smem_u32(&empty_bar[s]), 0x3);
+          }
+          umma_commit_pair(smem_u32(&accf_bar[acc]), 0x3);
         }
-        umma_commit(smem_u32(&accf_bar[acc]));
       }
     }
     __syncwarp();
@@ -248,14 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int k = 0;
       bool alive = true;
       for (int i = 0; i < my_tiles && alive; ++i) {
-        const TileCoord c =
-            tile_coord(p, static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x));
+        const TileCoord c = tile_coord(p, pair + i * n_pairs, rank);
+        if (c.t0 >= p.T) continue;  // no rows of this CTA in the tile
         for (int ch = 0; ch < kChunks && alive; ++ch) {
           const int hc = c.h0 + ch * kChunk;
           if (!chunk_active(p, hc)) continue;
           for (int pp = 0; pp < p.P; ++pp, ++k) {
-            const int s = k % kSlots;
-            const uint32_t round = static_cast<uint32_t>(k / kSlots);
+            const int s = k % n_slots;
+            const uint32_t round = static_cast<uint32_t>(k / n_slots);
             if (!mbar_wait(smem_u32(&sempty_bar[s]), (round & 1u) ^ 1u, p.err, abort_v)) {
               alive = false;
               break;
@@ -268,39 +284,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (*abort_v) {
-        for (int kk = max(0, k - kSlots); kk < k; ++kk)
-          wait_drain(smem_u32(&sfull_bar[kk % kSlots]), static_cast<uint32_t>(kk / kSlots) & 1u);
+        for (int kk = max(0, k - n_slots); kk < k; ++kk)
+          wait_drain(smem_u32(&sfull_bar[kk % n_slots]), static_cast<uint32_t>(kk / n_slots) & 1u);
       }
     }
     __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     const int q = warp & 3;       // TMEM lane quadrant this warp may access
-    const int r = q * 32 + lane;  // token row within the tile
+    const int r = q * 32 + lane;  // token row within this CTA's half of the tile
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int k = 0;
     bool alive = true;
     for (int i = 0; i < my_tiles && alive; ++i) {
       const int acc = i & 1;
       const uint32_t use = static_cast<uint32_t>(i >> 1);
-      const TileCoord c =
-          tile_coord(p, static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x));
+      const TileCoord c = tile_coord(p, pair + i * n_pairs, rank);
       const int t = c.t0 + r;
       const bool row_ok = t < p.T;
+      const bool has_rows = c.t0 < p.T;
       const uint32_t dcol = tmem + lane_base + static_cast<uint32_t>(acc * kTileH);
       bool acc_ready = false;
 #pragma unroll 1
       for (int ch = 0; ch < kChunks; ++ch) {
         const int hc = c.h0 + ch * kChunk;
-        const bool active = chunk_active(p, hc);
+        const bool active = has_rows && chunk_active(p, hc);
         float s[kChunk];
 #pragma unroll
         for (int j = 0; j < kChunk; ++j) s[j] = 0.f;
         if (active) {
           // sum the P partial boxes of this chunk, p ascending
           for (int pp = 0; pp < p.P; ++pp, ++k) {
-            const int sl = k % kSlots;
-            const uint32_t round = static_cast<uint32_t>(k / kSlots);
+            const int sl = k % n_slots;
+            const uint32_t round = static_cast<uint32_t>(k / n_slots);
             bool ok = mbar_wait(smem_u32(&sfull_bar[sl]), round & 1u, p.err, abort_v);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
@@ -319,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!alive) break;
         }
         if (!acc_ready) {
-          bool ok = mbar_wait(smem_u32(&accf_bar[acc]), use & 1u, p.err, abort_v);
+          bool ok = mbar_wait_cluster(smem_u32(&accf_bar[acc]), use & 1u, p.err, abort_v);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) {
             alive = false;
@@ -332,9 +348,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();  // tcgen05.ld needs the whole warp converged
         tmem_ld32(dcol + static_cast<uint32_t>(ch * kChunk), v0);
         tmem_ld32(dcol + static_cast<uint32_t>(ch * kChunk + 32), v1);
-        if (ch == kChunks - 1) {  // accumulator fully read: hand it back to the MMA warp
+        if (ch == kChunks - 1) {  // accumulator fully read: hand it back to the MMA issuer
           tc_fence_before();
-          mbar_arrive(smem_u32(&acce_bar[acc]));
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t bar = smem_u32(&acce_bar[acc]);
+            if (rank == 0)
+              mbar_arrive(bar);
+            else
+              mbar_arrive_remote(map_to_rank(bar, 0));
+          }
         }
         if (!active || !row_ok) continue;
         uint16_t* dst = p.out + static_cast<size_t>(t) * p.H + hc;
@@ -355,17 +378,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // Neither CTA may leave while the pair's MMAs could still read its shared
+  // memory or write its TMEM, or while its peer could still signal it.
   tc_fence_before();
   __syncthreads();
+  if (warp == 1 && rank == 0 && *abort_v && lane == 0) {
+    const int last = my_tiles - 1;
+    for (int i = max(0, last - 1); i <= last; ++i)
+      wait_drain(smem_u32(&accf_bar[i & 1]), static_cast<uint32_t>(i >> 1) & 1u);
+  }
+  __syncwarp();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    if (*abort_v && lane == 0) {  // no MMA may still write TMEM when it is freed
-      const int last = my_tiles - 1;
-      for (int i = max(0, last - 1); i <= last; ++i)
-        wait_drain(smem_u32(&accf_bar[i & 1]), static_cast<uint32_t>(i >> 1) & 1u);
-    }
-    __syncwarp();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
@@ -397,7 +423,7 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   p.col_end = a.col_end;
   p.htile0 = a.col_start / kTileH;
   p.n_htiles = (a.col_end - 1) / kTileH - p.htile0 + 1;
-  p.n_ttiles = ceil_div(a.T, kTileT);
+  p.n_tpairs = ceil_div(a.T, 2 * kTileT);
   p.total_kb = ceil_div(a.L, kBlockK);
   p.stages = kDefaultStages;
   p.slots = kDefaultSlots;
@@ -409,8 +435,8 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   if (smem > kSmemLimit) return cudaErrorInvalidConfiguration;
   p.pdl = a.pdl ? 1 : 0;
   p.err = dev.err_word;
-  const long long tiles = static_cast<long long>(p.n_htiles) * p.n_ttiles;
-  const int grid = static_cast<int>(std::min<long long>(dev.num_sms, tiles));
+  const long long tiles = static_cast<long long>(p.n_htiles) * p.n_tpairs;
+  const int grid = 2 * static_cast<int>(std::min<long long>(dev.num_sms / 2, tiles));
 
   // The shared partials as one 2-D tensor [P*T rows, H columns]: the box for
   // (partial p, tokens t0..t0+127) starts at row p*T + t0. Rows past T inside
@@ -418,7 +444,7 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   // and columns past H read as zero.
   CUtensorMap y_map, w_map, s_map;
   if (!make_map_bf16_sw128(&y_map, a.y, a.T, a.L, kTileT)) return cudaErrorInvalidValue;
-  if (!make_map_bf16_sw128(&w_map, a.W, a.H, a.L, kTileH)) return cudaErrorInvalidValue;
+  if (!make_map_bf16_sw128(&w_map, a.W, a.H, a.L, kHalfH)) return cudaErrorInvalidValue;
   if (!make_map_bf16_sw128(&s_map, a.shared, static_cast<uint64_t>(a.P) * a.T, a.H, kTileT))
     return cudaErrorInvalidValue;
 
@@ -427,8 +453,13 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
   int n = 0;
+  attrs[n].id = cudaLaunchAttributeClusterDimension;  // CTA pairs
+  attrs[n].val.clusterDim.x = 2;
+  attrs[n].val.clusterDim.y = 1;
+  attrs[n].val.clusterDim.z = 1;
+  ++n;
   if (a.pdl) {
     attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attrs[n].val.programmaticStreamSerializationAllowed = 1;
