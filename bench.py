@@ -369,12 +369,21 @@ def ours(args):
     fl = flops(T, L, H)
     proj_gbs = pb / (us_proj * 1e-6) / 1e9
     call_gbs = cb / (us_call * 1e-6) / 1e9
-    bound = "hbm"
-    roof = {"kernel": "decode_kernel" if T <= 128 else "prefill_kernel", "bound": bound,
-            "achieved": round(proj_gbs, 1), "peak": hbm, "unit": "GB/s",
-            "frac": round(proj_gbs / hbm, 4), "traffic": None,
-            "algorithmic_bytes_per_launch": pb, "us_per_launch": round(us_proj, 3),
-            "peak_source": peak_kind}
+    # The binding roofline of the projection kernel: HBM unless its flops take
+    # longer at the tensor peak than its bytes at the HBM peak (P = 1 prefill).
+    tensor_bound = fl / (tc_burst * 1e12) > pb / (hbm * 1e9)
+    kname = "decode_kernel" if T <= 128 else "prefill_kernel"
+    if tensor_bound:
+        proj_tf = fl / (us_proj * 1e-6) / 1e12
+        roof = {"kernel": kname, "bound": "tensor", "achieved": round(proj_tf, 1),
+                "peak": tc_burst, "unit": "TFLOP/s", "frac": round(proj_tf / tc_burst, 4),
+                "traffic": None, "algorithmic_flops_per_launch": fl,
+                "us_per_launch": round(us_proj, 3), "peak_source": peak_kind}
+    else:
+        roof = {"kernel": kname, "bound": "hbm", "achieved": round(proj_gbs, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(proj_gbs / hbm, 4), "traffic": None,
+                "algorithmic_bytes_per_launch": pb, "us_per_launch": round(us_proj, 3),
+                "peak_source": peak_kind}
     call_roof = {"achieved": round(call_gbs, 1), "peak": hbm, "unit": "GB/s",
                  "frac": round(call_gbs / hbm, 4), "algorithmic_bytes_per_call": cb,
                  "tensor_tflops": round(fl / (us_call * 1e-6) / 1e12, 2),

@@ -82,11 +82,17 @@ LT_API size_t latent_tail_workspace_size(int P, int T, int L, int H);
  * with col_start = 0, col_end = H).
  *   routed      [P, T, L] bf16  routed-expert latent partials
  *   shared      [P, T, H] bf16  shared-expert output partials
- *   norm_weight [L]       fp32  RMSNorm weight g
+ *   norm_weight [L]       fp32  RMSNorm weight g, or NULL for the pages'
+ *                               `transform.norm is None` branch: no RMSNorm, the
+ *                               latent is the partial sum itself (eps unused)
  *   W           [H, L]    bf16  up-projection weight (row h = output column h)
  *   out         [T, H]    bf16  result, round-to-nearest-even; must not overlap
- *                               any input or the workspace
- *   eps                         RMSNorm epsilon, finite and > 0
+ *                               routed, W, g or the workspace. It may be exactly
+ *                               one of the shared partials (out == shared + p*T*H):
+ *                               the pages' in-place `addmm_` into the shared
+ *                               output; any other overlap with shared is rejected
+ *   eps                         RMSNorm epsilon, finite and > 0 (when norm_weight
+ *                               is not NULL)
  *   workspace, workspace_bytes  at least latent_tail_workspace_size(P,T,L,H)
  *                               bytes of device scratch; its contents on entry
  *                               are ignored and on return are unspecified
@@ -118,7 +124,7 @@ LT_API lt_status latent_tail_forward_cols(const uint16_t* routed, const uint16_t
 /*
  * Steps 1-2 alone (the pages' `allreduce_norm_latent_out`): latent[t,l] =
  * bf16_rn(x[t,l] * rsqrt(mean_l x^2 + eps) * g[l]) with x = sum_p routed[p,t,l]
- * accumulated in FP32.
+ * accumulated in FP32; with norm_weight == NULL, latent = bf16_rn(x).
  *   routed [P, T, L] bf16, norm_weight [L] fp32, latent [T, L] bf16 (output,
  *   must not overlap the inputs).
  */
@@ -130,7 +136,8 @@ LT_API lt_status latent_tail_norm(const uint16_t* routed, const float* norm_weig
  * Steps 3-5 alone (the pages' narrowed `addmm_` beta-add plus the shared-partial
  * sum): out[t,h] = bf16_rn(sum_l latent[t,l] * W[h,l] + sum_p shared[p,t,h]) for
  * col_start <= h < col_end; other columns untouched.
- *   latent [T, L] bf16, shared [P, T, H] bf16, W [H, L] bf16, out [T, H] bf16.
+ *   latent [T, L] bf16, shared [P, T, H] bf16, W [H, L] bf16, out [T, H] bf16
+ *   (out may be exactly one of the shared partials, as in latent_tail_forward).
  * Range rules as in latent_tail_forward_cols; results are bit-identical to the
  * projection step of latent_tail_forward given the same latent. With P = 1 this
  * is the per-rank compute after the reference's all-reduce.

@@ -99,9 +99,11 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _dev(t, name: str, dtype, ndim: int):
+def _dev(t, name: str, dtype, ndim: int, optional: bool = False):
     import torch
 
+    if t is None and optional:
+        return None
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype or t.dim() != ndim:
@@ -130,14 +132,15 @@ def latent_tail_forward_cols(routed, shared, norm_weight, W, out, eps: float,
     bf = torch.bfloat16
     r = _dev(routed, "routed", bf, 3)
     s = _dev(shared, "shared", bf, 3)
-    g = _dev(norm_weight, "norm_weight", torch.float32, 1)
+    g = _dev(norm_weight, "norm_weight", torch.float32, 1, optional=True)
     w = _dev(W, "W", bf, 2)
     o = _dev(out, "out", bf, 2)
     ws = _dev(workspace, "workspace", workspace.dtype, workspace.dim())
     P, T, L = routed.shape
     H = W.shape[0]
     if tuple(shared.shape) != (P, T, H) or tuple(W.shape) != (H, L) \
-            or tuple(out.shape) != (T, H) or tuple(norm_weight.shape) != (L,):
+            or tuple(out.shape) != (T, H) \
+            or (norm_weight is not None and tuple(norm_weight.shape) != (L,)):
         raise ValueError("inconsistent shapes: routed [P,T,L], shared [P,T,H], W [H,L], "
                          "out [T,H], norm_weight [L]")
     nbytes = workspace.numel() * workspace.element_size()
@@ -156,10 +159,11 @@ def latent_tail_norm(routed, norm_weight, latent, eps: float, stream=None) -> No
     import torch
 
     r = _dev(routed, "routed", torch.bfloat16, 3)
-    g = _dev(norm_weight, "norm_weight", torch.float32, 1)
+    g = _dev(norm_weight, "norm_weight", torch.float32, 1, optional=True)
     y = _dev(latent, "latent", torch.bfloat16, 2)
     P, T, L = routed.shape
-    if tuple(latent.shape) != (T, L) or tuple(norm_weight.shape) != (L,):
+    if tuple(latent.shape) != (T, L) or (norm_weight is not None
+                                         and tuple(norm_weight.shape) != (L,)):
         raise ValueError("inconsistent shapes: routed [P,T,L], latent [T,L], norm_weight [L]")
     _check(load_library().latent_tail_norm(r, g, y, P, T, L, float(eps),
                                            _stream_handle(stream)), "latent_tail_norm")
@@ -194,13 +198,14 @@ def latent_tail_forward_noalloc(routed, shared, norm_weight, W, out, eps: float,
     bf = torch.bfloat16
     r = _dev(routed, "routed", bf, 3)
     s = _dev(shared, "shared", bf, 3)
-    g = _dev(norm_weight, "norm_weight", torch.float32, 1)
+    g = _dev(norm_weight, "norm_weight", torch.float32, 1, optional=True)
     w = _dev(W, "W", bf, 2)
     o = _dev(out, "out", bf, 2)
     P, T, L = routed.shape
     H = W.shape[0]
     if tuple(shared.shape) != (P, T, H) or tuple(W.shape) != (H, L) \
-            or tuple(out.shape) != (T, H) or tuple(norm_weight.shape) != (L,):
+            or tuple(out.shape) != (T, H) \
+            or (norm_weight is not None and tuple(norm_weight.shape) != (L,)):
         raise ValueError("inconsistent shapes: routed [P,T,L], shared [P,T,H], W [H,L], "
                          "out [T,H], norm_weight [L]")
     _check(load_library().latent_tail_forward_noalloc(r, s, g, w, o, P, T, L, H, float(eps),

@@ -87,6 +87,16 @@ Span span(const void* p, size_t bytes) {
 }
 bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
 
+// out may be exactly one of the P shared partials (in-place beta-add): every
+// kernel reads all partials of an output element before writing it, and no
+// other CTA reads that element.
+bool aliases_a_partial(const void* out, const void* shared, int P, int T, int H) {
+  const uintptr_t o = reinterpret_cast<uintptr_t>(out);
+  const uintptr_t s = reinterpret_cast<uintptr_t>(shared);
+  const uintptr_t plane = static_cast<uintptr_t>(T) * H * 2;
+  return o >= s && (o - s) % plane == 0 && (o - s) / plane < static_cast<uintptr_t>(P);
+}
+
 lt_status check_shape(int P, int T, int L, int H) {
   if (P < 1 || P > 64 || T < 0 || T > (1 << 24) || L < 8 || L > 16384 || H < 8 ||
       H > (1 << 20))
@@ -126,21 +136,23 @@ lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const flo
   lt_status st = check_shape(P, T, L, H);
   if (st != LT_OK) return st;
   if ((st = check_range(H, c0, c1)) != LT_OK) return st;
-  if (!std::isfinite(eps) || !(eps > 0.f)) return LT_ERR_INVALID_ARG;
+  if (g != nullptr && (!std::isfinite(eps) || !(eps > 0.f))) return LT_ERR_INVALID_ARG;
   if (T == 0) return LT_OK;
-  if ((st = check_ptrs({routed, shared, g, W, out})) != LT_OK) return st;
+  if ((st = check_ptrs({routed, shared, W, out})) != LT_OK) return st;
+  if (g != nullptr && !aligned16(g)) return LT_ERR_ALIGNMENT;
   const size_t need = latent_tail_workspace_size(P, T, L, H);
   if (ws == nullptr || ws_bytes < need) return LT_ERR_WORKSPACE;
   if (!aligned16(ws)) return LT_ERR_ALIGNMENT;
   const Span so = span(out, static_cast<size_t>(T) * H * 2);
   const Span sw = span(ws, need);
+  const Span ss = span(shared, static_cast<size_t>(P) * T * H * 2);
   const Span inputs[] = {span(routed, static_cast<size_t>(P) * T * L * 2),
-                         span(shared, static_cast<size_t>(P) * T * H * 2),
-                         span(g, static_cast<size_t>(L) * 4),
+                         span(g, g ? static_cast<size_t>(L) * 4 : 0),
                          span(W, static_cast<size_t>(H) * L * 2)};
   for (const Span& in : inputs)
     if (overlaps(so, in) || overlaps(sw, in)) return LT_ERR_INVALID_ARG;
-  if (overlaps(so, sw)) return LT_ERR_INVALID_ARG;
+  if (overlaps(sw, ss) || overlaps(so, sw)) return LT_ERR_INVALID_ARG;
+  if (overlaps(so, ss) && !aliases_a_partial(out, shared, P, T, H)) return LT_ERR_INVALID_ARG;
 
   const lt::DeviceInfo* dev = nullptr;
   if ((st = current_device(&dev)) != LT_OK) return st;
@@ -201,12 +213,13 @@ LT_API lt_status latent_tail_norm(const uint16_t* routed, const float* norm_weig
                                   lt_stream stream) {
   lt_status st = check_shape(P, T, L, 8);
   if (st != LT_OK) return st;
-  if (!std::isfinite(eps) || !(eps > 0.f)) return LT_ERR_INVALID_ARG;
+  if (norm_weight != nullptr && (!std::isfinite(eps) || !(eps > 0.f))) return LT_ERR_INVALID_ARG;
   if (T == 0) return LT_OK;
-  if ((st = check_ptrs({routed, norm_weight, latent})) != LT_OK) return st;
+  if ((st = check_ptrs({routed, latent})) != LT_OK) return st;
+  if (norm_weight != nullptr && !aligned16(norm_weight)) return LT_ERR_ALIGNMENT;
   const Span sy = span(latent, latent_bytes(T, L));
   if (overlaps(sy, span(routed, static_cast<size_t>(P) * T * L * 2)) ||
-      overlaps(sy, span(norm_weight, static_cast<size_t>(L) * 4)))
+      overlaps(sy, span(norm_weight, norm_weight ? static_cast<size_t>(L) * 4 : 0)))
     return LT_ERR_INVALID_ARG;
   const lt::DeviceInfo* dev = nullptr;
   if ((st = current_device(&dev)) != LT_OK) return st;
@@ -224,8 +237,10 @@ LT_API lt_status latent_tail_project_cols(const uint16_t* latent, const uint16_t
   if ((st = check_ptrs({latent, shared, W, out})) != LT_OK) return st;
   const Span so = span(out, static_cast<size_t>(T) * H * 2);
   if (overlaps(so, span(latent, latent_bytes(T, L))) ||
-      overlaps(so, span(shared, static_cast<size_t>(P) * T * H * 2)) ||
       overlaps(so, span(W, static_cast<size_t>(H) * L * 2)))
+    return LT_ERR_INVALID_ARG;
+  if (overlaps(so, span(shared, static_cast<size_t>(P) * T * H * 2)) &&
+      !aliases_a_partial(out, shared, P, T, H))
     return LT_ERR_INVALID_ARG;
   const lt::DeviceInfo* dev = nullptr;
   if ((st = current_device(&dev)) != LT_OK) return st;

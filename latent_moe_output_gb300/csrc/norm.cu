@@ -1,5 +1,7 @@
 // Steps 1-2 of the latent-MoE tail: sum the P routed partials of each token in
-// FP32 and apply RMSNorm with weight g, writing the bf16 latent y[T,L].
+// FP32 and apply RMSNorm with weight g, writing the bf16 latent y[T,L]. With no
+// weight (g == nullptr, the pages' `transform.norm is None` branch) the latent
+// is the partial sum itself.
 //
 // Follows `allreduce_norm_latent_out` in PR #50383's `_shard_up_proj_tail`
 // (all-reduce first, then the norm) and F.rms_norm as the PR #51253 test
@@ -83,8 +85,20 @@ __global__ void __launch_bounds__(kNormThreads)
   __syncthreads();
   const float r = 1.0f / sqrtf(red[0] / static_cast<float>(L) + eps);
 
-  const float4* g4 = reinterpret_cast<const float4*>(g);
   uint4* dst = reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * L);
+  if (g == nullptr) {  // no norm: round the partial sum itself
+    for (int c = threadIdx.x; c < nchunk; c += kNormThreads) {
+      const float4 x0 = xs4[2 * c], x1 = xs4[2 * c + 1];
+      uint4 o;
+      o.x = pack_bf16x2(x0.x, x0.y);
+      o.y = pack_bf16x2(x0.z, x0.w);
+      o.z = pack_bf16x2(x1.x, x1.y);
+      o.w = pack_bf16x2(x1.z, x1.w);
+      dst[c] = o;
+    }
+    return;
+  }
+  const float4* g4 = reinterpret_cast<const float4*>(g);
   for (int c = threadIdx.x; c < nchunk; c += kNormThreads) {
     const float4 x0 = xs4[2 * c], x1 = xs4[2 * c + 1];
     const float4 g0 = __ldg(g4 + 2 * c), g1 = __ldg(g4 + 2 * c + 1);

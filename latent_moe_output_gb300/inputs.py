@@ -53,8 +53,11 @@ DECODE_SWEEP = tuple(
 )
 PREFILL = Workload("prefill", P=8, T=8192, L=2048, H=7168, seed=2)
 STRESS = Workload("stress", P=16, T=16384, L=2048, H=7168, seed=3, outlier_rows=True)
+# One routed and one shared partial: the per-rank work after the reference's
+# all-reduce (tensor-core bound rather than bandwidth bound).
+PREFILL_P1 = Workload("prefill_p1", P=1, T=8192, L=2048, H=7168, seed=4)
 
-WORKLOADS = {w.name: w for w in (TINY, DECODE, *DECODE_SWEEP, PREFILL, STRESS)}
+WORKLOADS = {w.name: w for w in (TINY, DECODE, *DECODE_SWEEP, PREFILL, STRESS, PREFILL_P1)}
 
 # Column shards of the stress workload: 16 equal ranges of H.
 STRESS_SHARDS = 16

@@ -86,24 +86,27 @@ def _bf16_bits(a) -> np.ndarray:
     return a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def _f32(a) -> np.ndarray:
+def _f32(a) -> np.ndarray | None:
+    if a is None:
+        return None
     if isinstance(a, np.ndarray):
         return np.ascontiguousarray(a, dtype=np.float32)
     return a.detach().cpu().contiguous().float().numpy()
 
 
-def _ptr(a: np.ndarray) -> int:
-    return a.ctypes.data
+def _ptr(a: np.ndarray | None) -> int | None:
+    return None if a is None else a.ctypes.data
 
 
 def forward(routed, shared, g, W, eps: float, col_start: int = 0,
             col_end: int | None = None, precision: str = "f32", lib=None) -> np.ndarray:
-    """Oracle output [T, col_end-col_start] for routed [P,T,L], shared [P,T,H], W [H,L]."""
+    """Oracle output [T, col_end-col_start] for routed [P,T,L], shared [P,T,H], W [H,L].
+    g=None selects the no-norm branch (the latent is the routed partial sum)."""
     lib = lib or load()
     r, s, w, gg = _bf16_bits(routed), _bf16_bits(shared), _bf16_bits(W), _f32(g)
     P, T, L = r.shape
     H = w.shape[0]
-    if s.shape != (P, T, H) or w.shape != (H, L) or gg.shape != (L,):
+    if s.shape != (P, T, H) or w.shape != (H, L) or (gg is not None and gg.shape != (L,)):
         raise ValueError("shape mismatch between routed, shared, W and g")
     c1 = H if col_end is None else int(col_end)
     c0 = int(col_start)

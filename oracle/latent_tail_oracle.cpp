@@ -26,6 +26,9 @@
 //     shard, then the beta-add `hidden_shard.addmm_(latent, up_proj_shard.t())`.
 //   * RMSNorm as PyTorch's F.rms_norm defines it: x * rsqrt(mean(x^2) + eps) *
 //     weight, eps inside the square root, mean over the latent dimension.
+//   * the same source's branch for `transform.norm is None`: the latent is the
+//     all-reduced routed output itself. Here: g == NULL selects it (y = x, eps
+//     unused).
 //
 // Precision: the loop body is instantiated for float (the FP32 oracle the
 // parity tests use, matching the FP32 reference convention of PR #50593's
@@ -66,7 +69,7 @@ int check_args(const void* routed, const void* shared, const float* g,
                const void* out) {
   if (P < 1 || T < 0 || L < 1 || H < 1) return -1;
   if (c0 < 0 || c1 > H || c0 >= c1) return -2;
-  if (T > 0 && (!routed || !shared || !g || !W || !out)) return -3;
+  if (T > 0 && (!routed || !shared || !W || !out)) return -3;
   return 0;
 }
 
@@ -83,6 +86,18 @@ void normalized_latent(const uint16_t* routed, const float* g, long P, long T,
     for (long p = 0; p < P; ++p) s += widen_bf16(routed[((p * T) + t) * L + l]);
 #endif
     x[l] = s;
+  }
+  if (g == nullptr) {  // no norm: the latent is the partial sum itself
+#if LT_ORACLE_MUTANT == 10
+    // mistake: the no-norm branch still normalizes (with unit weight)
+    Acc ss0 = 0;
+    for (long l = 0; l < L; ++l) ss0 += x[l] * x[l];
+    const Acc r0 = static_cast<Acc>(1) / std::sqrt(ss0 / static_cast<Acc>(L) + eps);
+    for (long l = 0; l < L; ++l) y[l] = x[l] * r0;
+#else
+    for (long l = 0; l < L; ++l) y[l] = x[l];
+#endif
+    return;
   }
   Acc ss = 0;
 #if LT_ORACLE_MUTANT == 9
@@ -157,7 +172,7 @@ template <typename Acc>
 int latent(const uint16_t* routed, const float* g, long P, long T, long L,
            double eps, Acc* y_out) {
   if (P < 1 || T < 0 || L < 1) return -1;
-  if (T > 0 && (!routed || !g || !y_out)) return -3;
+  if (T > 0 && (!routed || !y_out)) return -3;
   std::vector<Acc> x(L);
   for (long t = 0; t < T; ++t)
     normalized_latent<Acc>(routed, g, P, T, L, t, static_cast<Acc>(eps), x.data(),
@@ -170,7 +185,8 @@ int latent(const uint16_t* routed, const float* g, long P, long T, long L,
 extern "C" {
 
 // out[T, col_end-col_start] (row-major, FP32) for routed [P,T,L], shared
-// [P,T,H], W [H,L] given as bf16 bit patterns and g [L] in FP32.
+// [P,T,H], W [H,L] given as bf16 bit patterns and g [L] in FP32 (g == NULL:
+// no norm).
 int lt_oracle_forward_f32(const uint16_t* routed, const uint16_t* shared,
                           const float* g, const uint16_t* W, long P, long T,
                           long L, long H, double eps, long col_start,

@@ -18,6 +18,9 @@ test builds the oracle with planted mistakes and checks each one is caught):
 * brute_force       - 40-digit mpmath evaluation of the definition on tiny
                       inputs; the double oracle agrees to 1e-12 and the FP32
                       oracle to FP32 rounding
+* no_norm           - without a norm weight the latent is the plain partial
+                      sum: W = I gives out = sum_p routed + sum_p shared exactly,
+                      and a permuted selection matrix picks x[t, pi(h)]
 """
 
 from __future__ import annotations
@@ -194,5 +197,29 @@ def brute_force(lib):
     assert np.all(np.abs(got32 - want) <= bound), "FP32 oracle vs exact"
 
 
+def no_norm(lib):
+    gen = torch.Generator().manual_seed(18)
+    P, T, L = 3, 4, 32
+    # dyadic partials: every sum below is exact in FP32
+    routed = _bf16(torch.randint(-16, 17, (P, T, L), generator=gen).float() / 4)
+    shared = _bf16(torch.randint(-16, 17, (P, T, L), generator=gen).float() / 4)
+    x = _f(routed).sum(0)
+    s = _f(shared).sum(0)
+    W = torch.eye(L, dtype=BF16)
+    for prec in ("f32", "f64"):
+        got = oracle.forward(routed, shared, None, W, 1e-6, precision=prec, lib=lib)
+        assert np.array_equal(got, x + s), f"no-norm identity closed form ({prec})"
+    H = 24
+    pi = (5 * np.arange(H) + 1) % L
+    Wn = np.zeros((H, L), np.float32)
+    Wn[np.arange(H), pi] = 1.0
+    zeros = torch.zeros(P, T, H, dtype=BF16)
+    for prec in ("f32", "f64"):
+        got = oracle.forward(routed, zeros, None, _bf16(Wn), 1e-6, precision=prec, lib=lib)
+        assert np.array_equal(got, x[:, pi]), f"no-norm selection matrix ({prec})"
+        y = oracle.latent(routed, None, 1e-6, precision=prec, lib=lib)
+        assert np.array_equal(y, x), f"no-norm latent ({prec})"
+
+
 ALL_PINS = (g_zero, constant_row, selection_matrix, shared_linearity, p_split,
-            column_concat, brute_force)
+            column_concat, brute_force, no_norm)

@@ -107,6 +107,8 @@ def fwd(lib, routed=A, shared=B, g=C, W=D, out=E, P=2, T=4, L=64, H=128, eps=1e-
     (dict(eps=float("nan")), Status.INVALID_ARG),
     (dict(eps=float("inf")), Status.INVALID_ARG),
     (dict(routed=None), Status.INVALID_ARG),
+    (dict(g=None, routed=None), Status.INVALID_ARG),  # no-norm: other checks still apply
+    (dict(g=None, eps=0.0, out=E + 8), Status.ALIGNMENT),  # eps unused without a norm
     (dict(W=None), Status.INVALID_ARG),
     (dict(out=E + 8), Status.ALIGNMENT),
     (dict(g=C + 4), Status.ALIGNMENT),

@@ -57,7 +57,8 @@ def test_ragged_shapes(P, T, L, H):
     check_full(x, what=f"P{P} T{T} L{L} H{H}")
 
 
-@pytest.mark.parametrize("w", [inputs.PREFILL, inputs.STRESS], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [inputs.PREFILL, inputs.STRESS, inputs.PREFILL_P1],
+                         ids=lambda w: w.name)
 def test_full_size_sampled_rows(w):
     """Full BASELINE sizes on the device; the oracle checks every column of a
     sample of token rows: first and last rows, rows around tile edges, the
@@ -108,3 +109,23 @@ def test_zero_tokens():
     ws = torch.empty(256, dtype=torch.uint8, device="cuda")
     binding.latent_tail_forward(x.routed, x.shared, x.g, x.W, out, x.eps, ws)
     binding.latent_tail_check()
+
+
+@pytest.mark.parametrize("P,T,L,H", [(2, 5, 64, 128), (8, 16, 2048, 7168), (3, 300, 328, 1000)])
+def test_no_norm_branch(P, T, L, H):
+    """norm_weight = None: the latent is the routed partial sum itself (the
+    `transform.norm is None` branch of `_shard_up_proj_tail`)."""
+    import oracle
+
+    x = inputs.make(P, T, L, H, seed=77 + T)
+    xd = gh.to_dev(x)
+    got = binding.forward(xd.routed, xd.shared, None, xd.W, x.eps)
+    binding.latent_tail_check()
+    want = oracle.forward(x.routed, x.shared, None, x.W, x.eps)
+    gh.assert_parity(got, want, f"no-norm P{P} T{T} L{L} H{H}")
+    y = torch.empty(T, L, dtype=torch.bfloat16, device="cuda")
+    binding.latent_tail_norm(xd.routed, None, y, x.eps)
+    binding.latent_tail_check()
+    ywant = oracle.latent(x.routed, None, x.eps)
+    err = np.abs(y.float().cpu().numpy() - ywant)
+    assert np.all(err <= 2.0 ** -8 * np.abs(ywant) + 1e-6)

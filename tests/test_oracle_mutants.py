@@ -16,6 +16,7 @@ MUTANTS = {
     7: "shared partials read with the wrong layout",
     8: "W row taken relative to the column range",
     9: "squares of partials summed instead of the square of the sum",
+    10: "no-norm branch still normalizes",
 }
 
 
