@@ -12,6 +12,12 @@ timed with CUDA events on the launching stream, between a barrier and a device
 synchronize on both sides; with N > 1 each rank runs its own replica (token
 batches are independent, no collective) and the max time over ranks is used.
 
+The `e2e` figure times the same steps through the host-buffer entry point
+(latent_tail_forward_host): each step's partials start in page-locked host
+memory and its result ends there, inside the timed region. Next to it,
+`staged_copies_us_per_step` times explicit pinned-host <-> device copies around
+the device entry point.
+
 Prints one JSON line. `--impl reference` times the CPU oracle instead (the
 only other code path this file may run), on a bounded sample of the same
 workload.
@@ -334,28 +340,45 @@ def ours(args):
     t_proj = max_over_ranks(timed(project_only, args.steps), world)
     binding.latent_tail_check(stream)
 
-    # end to end: pinned host partials -> device -> tail -> host result, every step
+    # End to end through the host-buffer entry point: every step takes its
+    # partials from page-locked host memory and leaves its result there. Each
+    # input set has its own pinned host copy; steps rotate over them as the
+    # device-resident steps do, and are replayed from CUDA graphs the same way.
     e2e_steps = args.e2e_steps or min(args.steps, 500)
-    hx = sets[0][0]
-    h_routed = hx.routed.cpu().pin_memory()
-    h_shared = hx.shared.cpu().pin_memory()
+    hsets = [(x.routed.cpu().pin_memory(), x.shared.cpu().pin_memory()) for x, _, _ in sets]
     h_out = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
-    d = {"routed": torch.empty_like(hx.routed), "shared": torch.empty_like(hx.shared),
-         "out": torch.empty(T, H, dtype=torch.bfloat16, device=dev),
-         "workspace": sets[0][2]}
+    h_ws = torch.empty(binding.latent_tail_host_workspace_size(P, T, L, H), dtype=torch.uint8,
+                       device=dev)
+
+    def e2e_step(i):
+        x = sets[i % n_sets][0]
+        hr, hs = hsets[i % n_sets]
+        binding.latent_tail_forward_host(hr, hs, x.g, x.W, h_out, x.eps, h_ws, stream)
+
+    # The same step with explicit staging copies issued from Python around the
+    # device entry point (pinned host -> device, call, device -> pinned host).
+    d_in = {"routed": torch.empty_like(sets[0][0].routed),
+            "shared": torch.empty_like(sets[0][0].shared),
+            "out": torch.empty(T, H, dtype=torch.bfloat16, device=dev)}
+
+    def staged_step(i):
+        x, _, ws = sets[i % n_sets]
+        hr, hs = hsets[i % n_sets]
+        d_in["routed"].copy_(hr, non_blocking=True)
+        d_in["shared"].copy_(hs, non_blocking=True)
+        binding.latent_tail_forward(d_in["routed"], d_in["shared"], x.g, x.W, d_in["out"],
+                                    x.eps, ws, stream)
+        h_out.copy_(d_in["out"], non_blocking=True)
+
     with torch.cuda.stream(stream):
-        for _ in range(3):
-            binding.forward_host(h_routed, h_shared, hx.g, hx.W, hx.eps, h_out, d, stream)
-        stream.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            binding.forward_host(h_routed, h_shared, hx.g, hx.W, hx.eps, h_out, d, stream)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+        for i in range(3):
+            e2e_step(i)
+    stream.synchronize()
+    t_e2e = max_over_ranks(timed(e2e_step, e2e_steps), world)
+    binding.latent_tail_check(stream)
+    if not torch.isfinite(h_out.float()).all():
+        raise RuntimeError("end-to-end steps did not produce a finite result")
+    t_staged = max_over_ranks(timed(staged_step, e2e_steps), world)
     binding.latent_tail_check(stream)
 
     if rank != 0:
@@ -405,7 +428,13 @@ def ours(args):
         "clocks": clocks.summary(),
         "e2e": {"value": round(job_throughput(T, e2e_steps, world, t_e2e), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": P * T * L * 2 + P * T * H * 2,
-                "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps},
+                "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps,
+                "us_per_step": round(t_e2e / e2e_steps * 1e6, 3),
+                "api": "latent_tail_forward_host (page-locked host partials and result; "
+                       + ("kernels read/write them across the host link"
+                          if T <= 128 else "staged with one copy per tensor") + ")",
+                "staged_copies_us_per_step": round(t_staged / e2e_steps * 1e6, 3),
+                "timing": "CUDA graphs, CUDA events, inputs rotate over pinned host sets"},
     }
     if not args.no_cpu_baseline and world >= 1:
         line["cpu_baseline"] = cpu_baseline(w)

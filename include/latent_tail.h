@@ -23,8 +23,9 @@
  *
  * Conventions for every entry point:
  *   - bf16 tensors are passed as `uint16_t*` holding bfloat16 bit patterns.
- *   - All arrays are DEVICE memory on the current CUDA device, contiguous and
- *     row-major, allocated and owned by the caller. Every pointer must be
+ *   - All arrays are DEVICE memory on the current CUDA device (except the
+ *     host buffers of latent_tail_forward_host), contiguous and row-major,
+ *     allocated and owned by the caller. Every pointer must be
  *     16-byte aligned. The library never allocates, frees or keeps a pointer
  *     after the call returns.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
@@ -194,6 +195,45 @@ LT_API lt_status latent_tail_forward_noalloc(const uint16_t* routed, const uint1
                                              const float* norm_weight, const uint16_t* W,
                                              uint16_t* out, int P, int T, int L, int H,
                                              float eps, lt_stream stream);
+
+/*
+ * Bytes of device workspace latent_tail_forward_host needs: the normalized
+ * latent as for latent_tail_workspace_size, plus, for T > 128, device staging
+ * for routed, shared and out (each rounded up to 256 bytes). Returns 0 for
+ * T <= 0 or invalid shapes. Host-only, never touches the GPU.
+ */
+LT_API size_t latent_tail_host_workspace_size(int P, int T, int L, int H);
+
+/*
+ * End-to-end form of latent_tail_forward for inputs that arrive in, and a
+ * result that leaves to, host memory (serving glue that holds the partials on
+ * the CPU side; the pages' tail always runs on device tensors, so this is a
+ * library convenience, not a step of the method).
+ *   routed_host [P, T, L], shared_host [P, T, H], out_host [T, H]: bf16 in
+ *     PAGE-LOCKED host memory mapped for the current device (cudaHostAlloc /
+ *     cudaMallocHost, or cudaHostRegister with cudaHostRegisterMapped), each
+ *     lying inside one such allocation, 16-byte aligned. Anything else
+ *     (pageable memory, device memory, a range running past its allocation)
+ *     gives LT_ERR_INVALID_ARG before any work is enqueued.
+ *   norm_weight, W: device memory, as in latent_tail_forward.
+ *   out_host: same overlap rules as out in latent_tail_forward (it may be
+ *     exactly one of the shared partials).
+ *   workspace: latent_tail_host_workspace_size(P, T, L, H) bytes of device
+ *     memory, not overlapping W or norm_weight.
+ * For T <= 128 the kernels read the partials and write the result through the
+ * host link directly: no staging copy, the host bytes cross the link once.
+ * Above, the partials are copied into the workspace (one cudaMemcpyAsync per
+ * tensor), the device path runs, and the result is copied back. Like every
+ * call it is asynchronous: out_host holds the result once `stream` has been
+ * synchronized, and the host buffers must not be modified before then.
+ * Results are bit-identical to latent_tail_forward on the same values.
+ */
+LT_API lt_status latent_tail_forward_host(const uint16_t* routed_host,
+                                          const uint16_t* shared_host,
+                                          const float* norm_weight, const uint16_t* W,
+                                          uint16_t* out_host, int P, int T, int L, int H,
+                                          float eps, void* workspace, size_t workspace_bytes,
+                                          lt_stream stream);
 
 /* Static, human-readable name of a status code. Never NULL. */
 LT_API const char* latent_tail_status_string(lt_status status);

@@ -17,9 +17,11 @@ from .binding import (  # noqa: F401
     latent_tail_check,
     latent_tail_forward,
     latent_tail_forward_cols,
+    latent_tail_forward_host,
     latent_tail_norm,
     latent_tail_project_cols,
     latent_tail_status_string,
+    latent_tail_host_workspace_size,
     latent_tail_workspace_size,
     library_path,
     load_library,

@@ -55,6 +55,10 @@ _SIGNATURES = {
     "latent_tail_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint, ctypes.c_void_p]),
     "latent_tail_forward_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4
                                     + [ctypes.c_float, ctypes.c_void_p]),
+    "latent_tail_host_workspace_size": (ctypes.c_size_t, [ctypes.c_int] * 4),
+    "latent_tail_forward_host": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4
+                                 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t,
+                                    ctypes.c_void_p]),
     "latent_tail_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -234,16 +238,66 @@ def forward(routed, shared, norm_weight, W, eps: float, col_start: int = 0,
     return out
 
 
-def forward_host(routed_host, shared_host, norm_weight, W, eps: float, out_host,
-                 dev_buffers: dict, stream=None):
-    """End-to-end call from pinned host buffers: copy this step's partials to the
-    device, run the tail, copy the result back into ``out_host``. ``dev_buffers``
-    holds the device tensors (routed, shared, out, workspace) reused per step;
-    ``norm_weight`` and ``W`` are resident model parameters on the device."""
-    d = dev_buffers
-    d["routed"].copy_(routed_host, non_blocking=True)
-    d["shared"].copy_(shared_host, non_blocking=True)
-    latent_tail_forward(d["routed"], d["shared"], norm_weight, W, d["out"], eps,
-                        d["workspace"], stream)
-    out_host.copy_(d["out"], non_blocking=True)
+def _host(t, name: str, dtype, ndim: int):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype or t.dim() != ndim:
+        raise TypeError(f"{name}: expected {ndim}-d {dtype}, got {t.dim()}-d {t.dtype}")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be in host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def latent_tail_host_workspace_size(P: int, T: int, L: int, H: int) -> int:
+    return int(load_library().latent_tail_host_workspace_size(P, T, L, H))
+
+
+def latent_tail_forward_host(routed_host, shared_host, norm_weight, W, out_host, eps: float,
+                             workspace, stream=None) -> None:
+    """Whole tail with routed/shared/out in page-locked host memory (the library
+    checks that they are; pageable memory is rejected) and W, g, workspace on the
+    device."""
+    import torch
+
+    bf = torch.bfloat16
+    r = _host(routed_host, "routed_host", bf, 3)
+    s = _host(shared_host, "shared_host", bf, 3)
+    o = _host(out_host, "out_host", bf, 2)
+    g = _dev(norm_weight, "norm_weight", torch.float32, 1, optional=True)
+    w = _dev(W, "W", bf, 2)
+    ws = _dev(workspace, "workspace", workspace.dtype, workspace.dim())
+    P, T, L = routed_host.shape
+    H = W.shape[0]
+    if tuple(shared_host.shape) != (P, T, H) or tuple(W.shape) != (H, L) \
+            or tuple(out_host.shape) != (T, H) \
+            or (norm_weight is not None and tuple(norm_weight.shape) != (L,)):
+        raise ValueError("inconsistent shapes: routed [P,T,L], shared [P,T,H], W [H,L], "
+                         "out [T,H], norm_weight [L]")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load_library().latent_tail_forward_host(r, s, g, w, o, P, T, L, H, float(eps), ws,
+                                                   nbytes, _stream_handle(stream)),
+           "latent_tail_forward_host")
+
+
+def forward_host(routed_host, shared_host, norm_weight, W, eps: float, out_host=None,
+                 workspace=None, stream=None):
+    """End-to-end call on page-locked host tensors: allocate ``out_host``
+    (pinned) and the device workspace with torch when not given, run the tail
+    through latent_tail_forward_host and return ``out_host`` (valid once the
+    stream is synchronized)."""
+    import torch
+
+    P, T, L = routed_host.shape
+    H = W.shape[0]
+    if out_host is None:
+        out_host = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    if workspace is None:
+        n = latent_tail_host_workspace_size(P, T, L, H)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=W.device)
+    latent_tail_forward_host(routed_host, shared_host, norm_weight, W, out_host, eps,
+                             workspace, stream)
     return out_host

@@ -25,6 +25,9 @@ struct DeviceSlot {
 DeviceSlot g_devices[kMaxDevices];
 std::mutex g_mutex;
 
+typedef CUresult (*PointerGetAttributeFn)(void*, CUpointer_attribute, CUdeviceptr);
+PointerGetAttributeFn g_ptr_attr = nullptr;
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -54,6 +57,15 @@ lt_status init_device(int dev, DeviceSlot& slot) {
         q != cudaDriverEntryPointSuccess || fn == nullptr)
       return LT_ERR_CUDA;
     g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  if (g_ptr_attr == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return LT_ERR_CUDA;
+    g_ptr_attr = reinterpret_cast<PointerGetAttributeFn>(fn);
   }
   if (lt::setup_norm(d) != cudaSuccess || lt::setup_decode(d) != cudaSuccess ||
       lt::setup_prefill(d) != cudaSuccess)
@@ -95,6 +107,28 @@ bool aliases_a_partial(const void* out, const void* shared, int P, int T, int H)
   const uintptr_t s = reinterpret_cast<uintptr_t>(shared);
   const uintptr_t plane = static_cast<uintptr_t>(T) * H * 2;
   return o >= s && (o - s) % plane == 0 && (o - s) / plane < static_cast<uintptr_t>(P);
+}
+
+// Device address through which the current device reaches the page-locked
+// host range [p, p + bytes), or nullptr when the range is not entirely inside
+// one page-locked host allocation or registration mapped for this device.
+// Queries only; never touches the memory.
+void* mapped_host_range(const void* p, size_t bytes) {
+  if (p == nullptr || bytes == 0 || g_ptr_attr == nullptr) return nullptr;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the (non-sticky) error the failed query recorded
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return nullptr;
+  CUdeviceptr start = 0;
+  size_t size = 0;
+  const CUdeviceptr q = static_cast<CUdeviceptr>(reinterpret_cast<uintptr_t>(p));
+  if (g_ptr_attr(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, q) != CUDA_SUCCESS ||
+      g_ptr_attr(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, q) != CUDA_SUCCESS)
+    return nullptr;
+  if (q < start || q - start > size || bytes > size - (q - start)) return nullptr;
+  return a.devicePointer;
 }
 
 lt_status check_shape(int P, int T, int L, int H) {
@@ -206,6 +240,69 @@ LT_API lt_status latent_tail_forward_cols(const uint16_t* routed, const uint16_t
                                           size_t workspace_bytes, lt_stream stream) {
   return forward_impl(routed, shared, norm_weight, W, out, P, T, L, H, eps, col_start, col_end,
                       workspace, workspace_bytes, stream);
+}
+
+LT_API size_t latent_tail_host_workspace_size(int P, int T, int L, int H) {
+  if (T <= 0 || check_shape(P, T, L, H) != LT_OK) return 0;
+  size_t b = round256(latent_bytes(T, L));
+  if (T > lt::kDecodeMaxTokens)  // staging for the partials and the result
+    b += round256(static_cast<size_t>(P) * T * L * 2) + round256(static_cast<size_t>(P) * T * H * 2) +
+         round256(static_cast<size_t>(T) * H * 2);
+  return b;
+}
+
+LT_API lt_status latent_tail_forward_host(const uint16_t* routed_host, const uint16_t* shared_host,
+                                          const float* norm_weight, const uint16_t* W,
+                                          uint16_t* out_host, int P, int T, int L, int H,
+                                          float eps, void* workspace, size_t workspace_bytes,
+                                          lt_stream stream) {
+  lt_status st = check_shape(P, T, L, H);
+  if (st != LT_OK) return st;
+  if (norm_weight != nullptr && (!std::isfinite(eps) || !(eps > 0.f))) return LT_ERR_INVALID_ARG;
+  if (T == 0) return LT_OK;
+  if ((st = check_ptrs({routed_host, shared_host, W, out_host})) != LT_OK) return st;
+  const size_t need = latent_tail_host_workspace_size(P, T, L, H);
+  if (workspace == nullptr || workspace_bytes < need) return LT_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return LT_ERR_ALIGNMENT;
+  if (norm_weight != nullptr && !aligned16(norm_weight)) return LT_ERR_ALIGNMENT;
+  const Span sw = span(workspace, need);
+  if (overlaps(sw, span(W, static_cast<size_t>(H) * L * 2)) ||
+      overlaps(sw, span(norm_weight, norm_weight ? static_cast<size_t>(L) * 4 : 0)))
+    return LT_ERR_INVALID_ARG;
+  const size_t r_bytes = static_cast<size_t>(P) * T * L * 2;
+  const size_t s_bytes = static_cast<size_t>(P) * T * H * 2;
+  const size_t o_bytes = static_cast<size_t>(T) * H * 2;
+  const Span so = span(out_host, o_bytes);
+  if (overlaps(so, span(routed_host, r_bytes))) return LT_ERR_INVALID_ARG;
+  if (overlaps(so, span(shared_host, s_bytes)) && !aliases_a_partial(out_host, shared_host, P, T, H))
+    return LT_ERR_INVALID_ARG;
+  const lt::DeviceInfo* dev = nullptr;
+  if ((st = current_device(&dev)) != LT_OK) return st;
+  void* rd = mapped_host_range(routed_host, r_bytes);
+  void* sd = mapped_host_range(shared_host, s_bytes);
+  void* od = mapped_host_range(out_host, o_bytes);
+  if (rd == nullptr || sd == nullptr || od == nullptr) return LT_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t y_bytes = round256(latent_bytes(T, L));
+  if (T <= lt::kDecodeMaxTokens) {
+    // The kernels read the partials and write the result across the host link.
+    return forward_impl(static_cast<const uint16_t*>(rd), static_cast<const uint16_t*>(sd),
+                        norm_weight, W, static_cast<uint16_t*>(od), P, T, L, H, eps, 0, H,
+                        workspace, y_bytes, stream);
+  }
+  // Larger calls: stage through device memory with one copy per tensor.
+  uint8_t* w8 = static_cast<uint8_t*>(workspace);
+  uint16_t* r_st = reinterpret_cast<uint16_t*>(w8 + y_bytes);
+  uint16_t* s_st = reinterpret_cast<uint16_t*>(w8 + y_bytes + round256(r_bytes));
+  uint16_t* o_st =
+      reinterpret_cast<uint16_t*>(w8 + y_bytes + round256(r_bytes) + round256(s_bytes));
+  if (cudaMemcpyAsync(r_st, routed_host, r_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(s_st, shared_host, s_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return LT_ERR_CUDA;
+  if ((st = forward_impl(r_st, s_st, norm_weight, W, o_st, P, T, L, H, eps, 0, H, workspace,
+                         y_bytes, stream)) != LT_OK)
+    return st;
+  return launch_status(cudaMemcpyAsync(out_host, o_st, o_bytes, cudaMemcpyDeviceToHost, s));
 }
 
 LT_API lt_status latent_tail_norm(const uint16_t* routed, const float* norm_weight,

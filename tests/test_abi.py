@@ -156,3 +156,48 @@ def test_binding_fails_loudly_without_library(tmp_path):
 def test_selftest_limit_validation(lib):
     assert lib.latent_tail_selftest_wait_timeout(0, None) == Status.INVALID_ARG
     assert lib.latent_tail_selftest_wait_timeout(1000001, None) == Status.INVALID_ARG
+
+
+def test_host_workspace_size(lib):
+    hws = lib.latent_tail_host_workspace_size
+    # decode sizes: the latent only (the kernels reach the host buffers directly)
+    assert hws(8, 16, 2048, 7168) == lib.latent_tail_workspace_size(8, 16, 2048, 7168)
+    assert hws(8, 128, 2048, 7168) == 128 * 2048 * 2
+    # above 128 tokens: latent + staging for routed, shared and out, each 256-rounded
+    P, T, L, H = 2, 129, 64, 128
+    r256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    assert hws(P, T, L, H) == r256(T * L * 2) + r256(P * T * L * 2) + r256(P * T * H * 2) \
+        + r256(T * H * 2)
+    assert hws(8, 0, 2048, 7168) == 0
+    assert hws(8, 16, 2047, 7168) == 0
+
+
+def fwd_host(lib, routed=A, shared=B, g=C, W=D, out=E, P=2, T=4, L=64, H=128, eps=1e-6,
+             ws=WS, wsb=1 << 20):
+    return lib.latent_tail_forward_host(routed, shared, g, W, out, P, T, L, H, eps, ws, wsb,
+                                        None)
+
+
+@pytest.mark.parametrize("kwargs,expect", [
+    (dict(P=0), Status.INVALID_ARG),
+    (dict(L=60), Status.ALIGNMENT),
+    (dict(eps=0.0), Status.INVALID_ARG),
+    (dict(routed=None), Status.INVALID_ARG),
+    (dict(out=None), Status.INVALID_ARG),
+    (dict(W=None), Status.INVALID_ARG),
+    (dict(routed=A + 8), Status.ALIGNMENT),
+    (dict(ws=None), Status.WORKSPACE),
+    (dict(wsb=100), Status.WORKSPACE),
+    (dict(T=200, wsb=200 * 64 * 2 + 256), Status.WORKSPACE),  # staging not included
+    (dict(ws=WS + 8), Status.ALIGNMENT),
+    (dict(g=C + 4), Status.ALIGNMENT),
+    (dict(out=A + 64), Status.INVALID_ARG),   # out overlaps routed
+    (dict(out=B + 32), Status.INVALID_ARG),   # out straddles the shared partials
+    (dict(ws=D + 256), Status.INVALID_ARG),   # workspace overlaps W
+])
+def test_forward_host_validation(lib, kwargs, expect):
+    assert fwd_host(lib, **kwargs) == expect
+
+
+def test_forward_host_zero_tokens(lib):
+    assert fwd_host(lib, routed=None, shared=None, out=None, ws=None, T=0) == Status.OK
