@@ -6,7 +6,9 @@
 #include "latent_tail.h"
 #include "launch.h"
 
+#include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -159,6 +161,14 @@ size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
 lt_status launch_status(cudaError_t e) { return e == cudaSuccess ? LT_OK : LT_ERR_CUDA; }
 
+bool norm_prefetches_w() {
+#ifdef LT_TUNING
+  const char* v = std::getenv("LT_NORM_PREFETCH");
+  if (v) return std::atoi(v) != 0;
+#endif
+  return true;
+}
+
 lt_status run_project(const lt::ProjectArgs& a, const lt::DeviceInfo& dev, cudaStream_t s) {
   if (a.T <= lt::kDecodeMaxTokens) return launch_status(lt::launch_decode(a, dev, s));
   return launch_status(lt::launch_prefill(a, dev, s));
@@ -166,7 +176,8 @@ lt_status run_project(const lt::ProjectArgs& a, const lt::DeviceInfo& dev, cudaS
 
 lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const float* g,
                        const uint16_t* W, uint16_t* out, int P, int T, int L, int H, float eps,
-                       int c0, int c1, void* ws, size_t ws_bytes, lt_stream stream) {
+                       int c0, int c1, void* ws, size_t ws_bytes, lt_stream stream,
+                       bool early_trigger = true) {
   lt_status st = check_shape(P, T, L, H);
   if (st != LT_OK) return st;
   if ((st = check_range(H, c0, c1)) != LT_OK) return st;
@@ -192,9 +203,17 @@ lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const flo
   if ((st = current_device(&dev)) != LT_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint16_t* y = static_cast<uint16_t*>(ws);
-  const lt::NormArgs na{routed, g, y, P, T, L, eps};
+  lt::NormArgs na{routed, g, y, P, T, L, eps, nullptr, 0};
+  if (T <= lt::kDecodeMaxTokens && norm_prefetches_w()) {
+    // The decode kernel streams W in whole 128-row tiles covering [c0, c1).
+    const int r0 = c0 / lt::kDecodeTileRows * lt::kDecodeTileRows;
+    const int r1 = std::min(H, (c1 + lt::kDecodeTileRows - 1) / lt::kDecodeTileRows *
+                                   lt::kDecodeTileRows);
+    na.l2_prefetch = W + static_cast<size_t>(r0) * L;
+    na.l2_prefetch_bytes = static_cast<size_t>(r1 - r0) * L * 2;
+  }
   if ((st = launch_status(lt::launch_norm(na, true, *dev, s))) != LT_OK) return st;
-  const lt::ProjectArgs pa{y, shared, W, out, P, T, L, H, c0, c1, true};
+  const lt::ProjectArgs pa{y, shared, W, out, P, T, L, H, c0, c1, true, early_trigger};
   return run_project(pa, *dev, s);
 }
 
@@ -286,9 +305,11 @@ LT_API lt_status latent_tail_forward_host(const uint16_t* routed_host, const uin
   const size_t y_bytes = round256(latent_bytes(T, L));
   if (T <= lt::kDecodeMaxTokens) {
     // The kernels read the partials and write the result across the host link.
+    // Here the host link, not the W stream, bounds a call, and releasing the
+    // next call only after the MMAs measured faster than the early release.
     return forward_impl(static_cast<const uint16_t*>(rd), static_cast<const uint16_t*>(sd),
                         norm_weight, W, static_cast<uint16_t*>(od), P, T, L, H, eps, 0, H,
-                        workspace, y_bytes, stream);
+                        workspace, y_bytes, stream, /*early_trigger=*/false);
   }
   // Larger calls: stage through device memory with one copy per tensor.
   uint8_t* w8 = static_cast<uint8_t*>(workspace);
@@ -320,7 +341,7 @@ LT_API lt_status latent_tail_norm(const uint16_t* routed, const float* norm_weig
     return LT_ERR_INVALID_ARG;
   const lt::DeviceInfo* dev = nullptr;
   if ((st = current_device(&dev)) != LT_OK) return st;
-  const lt::NormArgs na{routed, norm_weight, latent, P, T, L, eps};
+  const lt::NormArgs na{routed, norm_weight, latent, P, T, L, eps, nullptr, 0};
   return launch_status(lt::launch_norm(na, false, *dev, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -341,7 +362,7 @@ LT_API lt_status latent_tail_project_cols(const uint16_t* latent, const uint16_t
     return LT_ERR_INVALID_ARG;
   const lt::DeviceInfo* dev = nullptr;
   if ((st = current_device(&dev)) != LT_OK) return st;
-  const lt::ProjectArgs pa{latent, shared, W, out, P, T, L, H, col_start, col_end, false};
+  const lt::ProjectArgs pa{latent, shared, W, out, P, T, L, H, col_start, col_end, false, false};
   return run_project(pa, *dev, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -31,7 +31,7 @@
 namespace lt {
 namespace {
 
-constexpr int kBlockM = 128;                              // W rows per tile
+constexpr int kBlockM = kDecodeTileRows;                  // W rows per tile
 constexpr int kBlockK = 64;                               // K per stage (128-byte rows)
 constexpr int kThreads = 192;                             // TMA, MMA, 4 epilogue warps
 constexpr int kEpiThreads = 128;
@@ -56,6 +56,7 @@ struct DecodeParams {
   uint32_t ssum_offset;  // byte offsets (from the 1024-aligned base) of the
   uint32_t slot_offset;  // shared-partial sums and of the received K-slice partials
   int pdl;
+  int trigger_after_issue;  // allow dependents once the last W copy is issued
   uint32_t* err;
 };
 
@@ -155,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(st + kWStageBytes, &y_map, fb, (kb_begin + i) * kBlockK, 0);
         issued = i + 1;
       }
+      if (p.trigger_after_issue) pdl_launch_dependents();
       if (*abort_v) {  // let copies already in flight land before the CTA exits
         for (int i = max(0, issued - p.stages); i < issued; ++i)
           wait_drain(smem_u32(&full_bar[i % p.stages]), static_cast<uint32_t>(i / p.stages) & 1u);
@@ -217,7 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below needs a converged warp
-    if (lane == 0 && warp == 2) pdl_launch_dependents();  // the next call may start its prologue
+    if (lane == 0 && warp == 2 && !p.trigger_after_issue)
+      pdl_launch_dependents();  // the next call may start its prologue
     const int q = warp & 3;            // TMEM lane quadrant of this warp
     const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
@@ -361,6 +364,10 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
       ring + ((static_cast<size_t>(p.npad) * rpc * 4 + 1023) & ~size_t(1023)));
   p.tmem_cols = next_pow2_at_least(p.npad, 32);
   p.pdl = a.pdl ? 1 : 0;
+  p.trigger_after_issue = a.early_trigger ? 1 : 0;
+#ifdef LT_TUNING
+  p.trigger_after_issue = env_int("LT_DECODE_TRIGGER", p.trigger_after_issue);
+#endif
   p.err = dev.err_word;
   const int tile_first = a.col_start / kBlockM;
   const int tile_last = (a.col_end - 1) / kBlockM;

@@ -33,7 +33,15 @@ struct NormArgs {
   uint16_t* y;             // [T,L]
   int P, T, L;
   float eps;
+  // Optional L2 prefetch, issued before the dependency wait, of the W rows the
+  // projection kernel streams next (l2_prefetch_bytes a multiple of 16).
+  const void* l2_prefetch;
+  size_t l2_prefetch_bytes;
 };
+
+// W rows per decode tile: the decode kernel reads W in whole tiles of this
+// many rows, starting at absolute multiples of it.
+constexpr int kDecodeTileRows = 128;
 
 struct ProjectArgs {
   const uint16_t* y;       // [T,L]
@@ -43,6 +51,10 @@ struct ProjectArgs {
   int P, T, L, H;
   int col_start, col_end;
   bool pdl;                // launched right after the norm kernel, may overlap it
+  // Decode kernel: let the next kernel on the stream launch as soon as each CTA
+  // has issued its last W copy (else once its MMAs are done). Earlier lets the
+  // next call's norm kernel prefetch its W into L2 during this call's tail.
+  bool early_trigger;
 };
 
 cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const DeviceInfo& dev,

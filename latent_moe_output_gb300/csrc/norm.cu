@@ -15,11 +15,14 @@
 #include "launch.h"
 #include "ptx.cuh"
 
+#include <algorithm>
+
 namespace lt {
 namespace {
 
 constexpr int kNormThreads = 256;
 constexpr int kMaxL = 16384;
+constexpr size_t kPrefetchPiece = 16384;
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -40,14 +43,27 @@ __device__ __forceinline__ void add8(float (&a)[8], const uint4& v) {
 
 __global__ void __launch_bounds__(kNormThreads)
     norm_kernel(const uint16_t* __restrict__ routed, const float* __restrict__ g,
-                uint16_t* __restrict__ y, int P, int T, int L, float eps, int trigger) {
+                uint16_t* __restrict__ y, int P, int T, int L, float eps, int trigger,
+                const uint8_t* __restrict__ pf, size_t pf_bytes) {
   extern __shared__ float4 xs4[];  // the token's x[L] in FP32
   __shared__ float red[kNormThreads / 32];
+  // Optional: pull the projection's W rows into L2 before waiting, spread over
+  // the CTAs of the grid first (piece i goes to CTA i % grid).
+  if (pf_bytes != 0) {
+    const size_t pieces = (pf_bytes + kPrefetchPiece - 1) / kPrefetchPiece;
+    for (size_t i = blockIdx.x + static_cast<size_t>(gridDim.x) * threadIdx.x; i < pieces;
+         i += static_cast<size_t>(gridDim.x) * kNormThreads) {
+      const size_t off = i * kPrefetchPiece;
+      const size_t n = pf_bytes - off < kPrefetchPiece ? pf_bytes - off : kPrefetchPiece;
+      l2_prefetch_bulk(pf + off, static_cast<uint32_t>(n));
+    }
+  }
   // Launched as a programmatic dependent of whatever precedes it on the stream:
   // wait for that work (it may produce `routed` or still read the latent buffer)
   // before touching memory, then let the projection kernel start its prologue.
   pdl_wait();
   if (trigger) pdl_launch_dependents();
+  if (static_cast<int>(blockIdx.x) >= T) return;  // CTAs that only prefetched
 
   const int t = blockIdx.x;
   const int nchunk = L >> 3;
@@ -118,10 +134,15 @@ cudaError_t setup_norm(const DeviceInfo&) {
                               kMaxL * static_cast<int>(sizeof(float)));
 }
 
-cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const DeviceInfo&,
+cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const DeviceInfo& dev,
                         cudaStream_t stream) {
+  if (a.l2_prefetch_bytes % 16 != 0 || reinterpret_cast<uintptr_t>(a.l2_prefetch) % 16 != 0)
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(a.T), 1, 1);
+  // With a prefetch, at least one CTA per SM so that every SM's copy engine
+  // issues a share of it.
+  const int grid = a.l2_prefetch_bytes != 0 ? std::max(a.T, dev.num_sms) : a.T;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kNormThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(a.L) * sizeof(float);
   cfg.stream = stream;
@@ -131,7 +152,8 @@ cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const Device
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, norm_kernel, a.routed, a.g, a.y, a.P, a.T, a.L, a.eps,
-                            trigger_dependents ? 1 : 0);
+                            trigger_dependents ? 1 : 0,
+                            static_cast<const uint8_t*>(a.l2_prefetch), a.l2_prefetch_bytes);
 }
 
 }  // namespace lt

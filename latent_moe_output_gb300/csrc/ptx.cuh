@@ -110,6 +110,15 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 }
 
 // ------------------------------------------------------------------ TMA
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned address) from
+// global memory into L2. Only a hint: L2 is where every access to this GPU's
+// memory is resolved, so a prefetch can never make a later load see stale data,
+// and it may be issued before waiting on the work that precedes the kernel.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+               ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
