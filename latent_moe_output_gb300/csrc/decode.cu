@@ -15,7 +15,11 @@
 //     is why the split stops at 4;
 //   * W boxes (128 x 64, 128-byte swizzle) are requested before the rest of the
 //     set-up, and under programmatic dependent launch before waiting for the
-//     norm kernel that writes y; one thread issues TMA, one issues tcgen05.mma;
+//     norm kernel that writes y (which has already prefetched W into L2); one
+//     thread issues TMA, one issues tcgen05.mma;
+//   * with early release, each CTA lets the next kernel on the stream launch
+//     once it has issued its last W copy, so the next call's norm kernel
+//     prefetches its W while this call finishes;
 //   * while W streams in, the epilogue warps sum the P shared partials of the
 //     rows this CTA finishes (p ascending, FP32) into shared memory;
 //   * after the MMAs, every CTA pushes each accumulator row into the shared
