@@ -76,6 +76,31 @@ def flops(T, L, width):
     return 2 * T * width * L
 
 
+def profiled_traffic(kernel, workload_name, T):
+    """DRAM bytes per launch of `kernel` (dram__bytes_read.sum + dram__bytes_write.sum)
+    from the ncu summary committed under profiles/, or None when no capture matches
+    this workload and token count, or the kernel's source changed since the capture
+    (its sha256 is recorded next to the figure)."""
+    import glob
+    import hashlib
+    import re
+
+    src = os.path.join(ROOT, "latent_moe_output_gb300", "csrc", kernel.replace("_kernel", "") + ".cu")
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    pat = re.compile(r"^traffic_per_launch_bytes: (\d+) \(workload (\w+), T (\d+), "
+                     r"(\S+) sha256 ([0-9a-f]{16})\)", re.M)
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", kernel + "_*.md"))):
+        with open(path) as f:
+            for m in pat.finditer(f.read()):
+                if (m.group(2) == workload_name and int(m.group(3)) == T
+                        and m.group(4) == os.path.basename(src) and m.group(5) == digest):
+                    return int(m.group(1))
+    return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -408,7 +433,8 @@ def ours(args):
                 "us_per_launch": round(us_proj, 3), "peak_source": peak_kind}
     else:
         roof = {"kernel": kname, "bound": "hbm", "achieved": round(proj_gbs, 1), "peak": hbm,
-                "unit": "GB/s", "frac": round(proj_gbs / hbm, 4), "traffic": None,
+                "unit": "GB/s", "frac": round(proj_gbs / hbm, 4),
+                "traffic": profiled_traffic(kname, w.name, T),
                 "algorithmic_bytes_per_launch": pb, "us_per_launch": round(us_proj, 3),
                 "peak_source": peak_kind}
     call_roof = {"achieved": round(call_gbs, 1), "peak": hbm, "unit": "GB/s",
