@@ -12,6 +12,10 @@ timed with CUDA events on the launching stream, between a barrier and a device
 synchronize on both sides; with N > 1 each rank runs its own replica (token
 batches are independent, no collective) and the max time over ranks is used.
 
+`single_call_us_median` is the median device time of one call with nothing else
+on the GPU before or after it (an eager call enqueued behind a spin kernel): the
+latency a single call sees, without the overlap between consecutive calls.
+
 The `e2e` figure times the same steps through the host-buffer entry point
 (latent_tail_forward_host): each step's partials start in page-locked host
 memory and its result ends there, inside the timed region. Next to it,
@@ -369,6 +373,25 @@ def ours(args):
     t_proj = max_over_ranks(timed(project_only, args.steps), world)
     binding.latent_tail_check(stream)
 
+    # One call at a time, with nothing before or after it on the GPU (no overlap
+    # with a neighbouring call): a spin kernel keeps the GPU busy while the
+    # events and the call's two kernel launches are enqueued, so the interval
+    # holds only the call's own device time.
+    single = []
+    with torch.cuda.stream(stream):
+        for i in range(max(100, 2 * n_sets) if T <= 128 else 3 * n_sets):
+            torch.cuda._sleep(200000)  # ~100 us at 2 GHz
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step(i)
+            b.record(stream)
+            b.synchronize()
+            if i >= n_sets:  # first round over the sets: warm-up
+                single.append(a.elapsed_time(b) * 1e3)
+    binding.latent_tail_check(stream)
+    us_single = max_over_ranks(statistics.median(single) * 1e-6, world) * 1e6
+
     # End to end through the host-buffer entry point: every step takes its
     # partials from page-locked host memory and leaves its result there. Each
     # input set has its own pinned host copy; steps rotate over them as the
@@ -445,6 +468,7 @@ def ours(args):
         "metric": "latent-tail tokens/s", "value": round(tokens_per_s, 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(t_step / args.steps * 1e3, 6), "us_per_call": round(us_call, 3),
+        "single_call_us_median": round(us_single, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "P": P, "T": T, "L": L, "H": H, "eps": inputs.EPS,
