@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--T", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps (capped)")
+    ap.add_argument("--shards", type=int, default=0,
+                    help="also time each step as N column-range calls covering [0, H)")
     return ap.parse_args()
 
 
@@ -117,7 +119,12 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region.
+
+    The sampler is started, and its first sample awaited, before the region
+    opens, so nvidia-smi's start-up does not eat into it. A region shorter than a
+    few sampling periods also takes the samples of the next 0.2 s (said so in
+    the summary)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -126,8 +133,17 @@ class ClockSampler:
     def __init__(self, device_index):
         self.dev = device_index
         self.proc = None
+        self.lines = []  # (host time, csv line)
+        self.t_open = self.t_close = 0.0
+
+    def _read(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.lines.append((time.perf_counter(), line))
 
     def __enter__(self):
+        import threading
+
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
@@ -135,23 +151,40 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        if self.proc is not None:
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            deadline = time.perf_counter() + 5.0
+            while not self.lines and time.perf_counter() < deadline:
+                time.sleep(0.005)
+        self.t_open = time.perf_counter()
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+        self.t_close = time.perf_counter()
+        if self.proc is None:
+            return
+        deadline = self.t_close + 0.2
+        while (time.perf_counter() < deadline
+               and sum(1 for t, _ in self.lines if t >= self.t_open) < 3):
+            time.sleep(0.005)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        self.reader.join(timeout=5)
 
     def summary(self):
+        inside = [l for t, l in self.lines if self.t_open <= t <= self.t_close + 0.03]
+        window = "timed region"
+        if len(inside) < 3:
+            inside = [l for t, l in self.lines if t >= self.t_open][:3]
+            window = "timed region and up to 0.2 s after it (region shorter than 3 samples)"
         sm, mx, reasons = [], None, set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in getattr(self, "lines", []):
+        for line in inside:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -164,7 +197,7 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "window": window}
 
 
 def dist_setup(n_gpus):
@@ -373,6 +406,26 @@ def ours(args):
     t_proj = max_over_ranks(timed(project_only, args.steps), world)
     binding.latent_tail_check(stream)
 
+    # Column-shard form: a step is N latent_tail_forward_cols calls whose ranges
+    # (multiples of 8) tile [0, H); together they write the whole output.
+    shard_line = None
+    if args.shards > 0:
+        bounds = [((H // 8) * k // args.shards) * 8 for k in range(args.shards)] + [H]
+
+        def shard_step(i):
+            x, out, ws = sets[i % n_sets]
+            for k in range(args.shards):
+                binding.latent_tail_forward_cols(x.routed, x.shared, x.g, x.W, out, x.eps,
+                                                 bounds[k], bounds[k + 1], ws, stream)
+
+        shard_steps = max(1, min(args.steps, 20))
+        t_shards = max_over_ranks(timed(shard_step, shard_steps), world)
+        binding.latent_tail_check(stream)
+        shard_line = {"calls_per_step": args.shards, "steps": shard_steps,
+                      "us_per_step": round(t_shards / shard_steps * 1e6, 3),
+                      "tokens_per_s": round(job_throughput(T, shard_steps, world, t_shards), 1),
+                      "note": "each call reduces and normalizes all T tokens again"}
+
     # One call at a time, with nothing before or after it on the GPU (no overlap
     # with a neighbouring call): a spin kernel keeps the GPU busy while the
     # events and the call's two kernel launches are enqueued, so the interval
@@ -469,6 +522,7 @@ def ours(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(t_step / args.steps * 1e3, 6), "us_per_call": round(us_call, 3),
         "single_call_us_median": round(us_single, 3),
+        **({"column_shards": shard_line} if shard_line else {}),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "P": P, "T": T, "L": L, "H": H, "eps": inputs.EPS,
