@@ -169,6 +169,14 @@ bool norm_prefetches_w() {
   return true;
 }
 
+bool norm_prefetches_routed() {
+#ifdef LT_TUNING
+  const char* v = std::getenv("LT_NORM_PF_ROUTED");
+  if (v) return std::atoi(v) != 0;
+#endif
+  return true;
+}
+
 lt_status run_project(const lt::ProjectArgs& a, const lt::DeviceInfo& dev, cudaStream_t s) {
   if (a.T <= lt::kDecodeMaxTokens) return launch_status(lt::launch_decode(a, dev, s));
   return launch_status(lt::launch_prefill(a, dev, s));
@@ -177,7 +185,7 @@ lt_status run_project(const lt::ProjectArgs& a, const lt::DeviceInfo& dev, cudaS
 lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const float* g,
                        const uint16_t* W, uint16_t* out, int P, int T, int L, int H, float eps,
                        int c0, int c1, void* ws, size_t ws_bytes, lt_stream stream,
-                       bool early_trigger = true) {
+                       bool early_trigger = true, bool routed_in_device_memory = true) {
   lt_status st = check_shape(P, T, L, H);
   if (st != LT_OK) return st;
   if ((st = check_range(H, c0, c1)) != LT_OK) return st;
@@ -203,14 +211,20 @@ lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const flo
   if ((st = current_device(&dev)) != LT_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint16_t* y = static_cast<uint16_t*>(ws);
-  lt::NormArgs na{routed, g, y, P, T, L, eps, nullptr, 0};
+  lt::NormArgs na{routed, g, y, P, T, L, eps, nullptr, 0, false};
   if (T <= lt::kDecodeMaxTokens && norm_prefetches_w()) {
     // The decode kernel streams W in whole 128-row tiles covering [c0, c1).
     const int r0 = c0 / lt::kDecodeTileRows * lt::kDecodeTileRows;
     const int r1 = std::min(H, (c1 + lt::kDecodeTileRows - 1) / lt::kDecodeTileRows *
                                    lt::kDecodeTileRows);
-    na.l2_prefetch = W + static_cast<size_t>(r0) * L;
-    na.l2_prefetch_bytes = static_cast<size_t>(r1 - r0) * L * 2;
+    const size_t w_bytes = static_cast<size_t>(r1 - r0) * L * 2;
+    if (w_bytes <= lt::kMaxWPrefetchBytes) {
+      na.l2_prefetch = W + static_cast<size_t>(r0) * L;
+      na.l2_prefetch_bytes = w_bytes;
+    }
+    // (not for page-locked host partials: the bulk L2 prefetch is only used on
+    // device memory)
+    na.prefetch_routed = routed_in_device_memory && norm_prefetches_routed();
   }
   if ((st = launch_status(lt::launch_norm(na, true, *dev, s))) != LT_OK) return st;
   const lt::ProjectArgs pa{y, shared, W, out, P, T, L, H, c0, c1, true, early_trigger};
@@ -309,7 +323,8 @@ LT_API lt_status latent_tail_forward_host(const uint16_t* routed_host, const uin
     // next call only after the MMAs measured faster than the early release.
     return forward_impl(static_cast<const uint16_t*>(rd), static_cast<const uint16_t*>(sd),
                         norm_weight, W, static_cast<uint16_t*>(od), P, T, L, H, eps, 0, H,
-                        workspace, y_bytes, stream, /*early_trigger=*/false);
+                        workspace, y_bytes, stream, /*early_trigger=*/false,
+                        /*routed_in_device_memory=*/false);
   }
   // Larger calls: stage through device memory with one copy per tensor.
   uint8_t* w8 = static_cast<uint8_t*>(workspace);
@@ -341,7 +356,7 @@ LT_API lt_status latent_tail_norm(const uint16_t* routed, const float* norm_weig
     return LT_ERR_INVALID_ARG;
   const lt::DeviceInfo* dev = nullptr;
   if ((st = current_device(&dev)) != LT_OK) return st;
-  const lt::NormArgs na{routed, norm_weight, latent, P, T, L, eps, nullptr, 0};
+  const lt::NormArgs na{routed, norm_weight, latent, P, T, L, eps, nullptr, 0, false};
   return launch_status(lt::launch_norm(na, false, *dev, reinterpret_cast<cudaStream_t>(stream)));
 }
 

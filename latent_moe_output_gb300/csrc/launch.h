@@ -37,7 +37,14 @@ struct NormArgs {
   // projection kernel streams next (l2_prefetch_bytes a multiple of 16).
   const void* l2_prefetch;
   size_t l2_prefetch_bytes;
+  // Also prefetch all of `routed` into L2 before the wait, ahead of W, so that
+  // its reads after the wait do not queue behind the W traffic.
+  bool prefetch_routed;
 };
+
+// Prefetches larger than these are skipped: they would not stay in L2.
+constexpr size_t kMaxRoutedPrefetchBytes = size_t(16) << 20;
+constexpr size_t kMaxWPrefetchBytes = size_t(64) << 20;
 
 // W rows per decode tile: the decode kernel reads W in whole tiles of this
 // many rows, starting at absolute multiples of it.

@@ -30,6 +30,7 @@ namespace {
 constexpr int kNormThreads = 256;
 constexpr int kMaxL = 16384;
 constexpr size_t kPrefetchPiece = 16384;
+constexpr size_t kRoutedPiece = 4096;  // small, so every SM issues one early
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -51,11 +52,25 @@ __device__ __forceinline__ void add8(float (&a)[8], const uint4& v) {
 __global__ void __launch_bounds__(kNormThreads)
     norm_kernel(const uint16_t* __restrict__ routed, const float* __restrict__ g,
                 uint16_t* __restrict__ y, int P, int T, int L, float eps, int trigger,
-                const uint8_t* __restrict__ pf, size_t pf_bytes) {
+                const uint8_t* __restrict__ pf, size_t pf_bytes, size_t pf_routed_bytes) {
   extern __shared__ float4 xs4[];  // the token's x[L] in FP32
   __shared__ float red[kNormThreads / 32];
-  // Optional: pull the projection's W rows into L2 before waiting, spread over
-  // the CTAs of the grid first (piece i goes to CTA i % grid).
+  // Optional: pull `routed` and then the projection's W rows into L2 before
+  // waiting, spread over the CTAs of the grid first (piece i goes to CTA
+  // i % grid). `routed` goes first on every SM so that its lines arrive before
+  // the W stream; if the preceding work is still writing it, the lines are
+  // simply updated in L2 and read after the wait below.
+  if (pf_routed_bytes != 0) {
+    const uint8_t* r8 = reinterpret_cast<const uint8_t*>(routed);
+    const size_t pieces = (pf_routed_bytes + kRoutedPiece - 1) / kRoutedPiece;
+    for (size_t i = blockIdx.x + static_cast<size_t>(gridDim.x) * threadIdx.x; i < pieces;
+         i += static_cast<size_t>(gridDim.x) * kNormThreads) {
+      const size_t off = i * kRoutedPiece;
+      const size_t n = pf_routed_bytes - off < kRoutedPiece ? pf_routed_bytes - off : kRoutedPiece;
+      l2_prefetch_bulk(r8 + off, static_cast<uint32_t>(n));
+    }
+    __syncthreads();
+  }
   if (pf_bytes != 0) {
     const size_t pieces = (pf_bytes + kPrefetchPiece - 1) / kPrefetchPiece;
     for (size_t i = blockIdx.x + static_cast<size_t>(gridDim.x) * threadIdx.x; i < pieces;
@@ -145,10 +160,14 @@ cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const Device
                         cudaStream_t stream) {
   if (a.l2_prefetch_bytes % 16 != 0 || reinterpret_cast<uintptr_t>(a.l2_prefetch) % 16 != 0)
     return cudaErrorInvalidValue;
+  const size_t routed_bytes = static_cast<size_t>(a.P) * a.T * a.L * 2;  // a multiple of 16
+  const size_t pf_routed =
+      a.prefetch_routed && routed_bytes <= kMaxRoutedPrefetchBytes ? routed_bytes : 0;
   cudaLaunchConfig_t cfg{};
   // With a prefetch, at least one CTA per SM so that every SM's copy engine
   // issues a share of it.
-  const int grid = a.l2_prefetch_bytes != 0 ? std::max(a.T, dev.num_sms) : a.T;
+  const int grid =
+      a.l2_prefetch_bytes != 0 || pf_routed != 0 ? std::max(a.T, dev.num_sms) : a.T;
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kNormThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(a.L) * sizeof(float);
@@ -160,7 +179,8 @@ cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const Device
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, norm_kernel, a.routed, a.g, a.y, a.P, a.T, a.L, a.eps,
                             trigger_dependents ? 1 : 0,
-                            static_cast<const uint8_t*>(a.l2_prefetch), a.l2_prefetch_bytes);
+                            static_cast<const uint8_t*>(a.l2_prefetch), a.l2_prefetch_bytes,
+                            pf_routed);
 }
 
 }  // namespace lt
