@@ -82,6 +82,9 @@ struct PrefillParams {
   int stages;       // operand ring depth
   int slots;        // shared-partial ring depth
   int pdl;
+  // Every pair owns at most one tile: the epilogue parks each chunk's shared sums
+  // in the idle second accumulator's TMEM columns while the mainloop runs.
+  int stage_sums;
   uint32_t* err;
 };
 
@@ -299,6 +302,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;       // TMEM lane quadrant this warp may access
     const int r = q * 32 + lane;  // token row within this CTA's half of the tile
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    // Accumulator `a` fully read by this warp: hand it back to the MMA issuer.
+    auto release_acc = [&](int a) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t bar = smem_u32(&acce_bar[a]);
+        if (rank == 0)
+          mbar_arrive(bar);
+        else
+          mbar_arrive_remote(map_to_rank(bar, 0));
+      }
+    };
+    // out[t, hc .. hc+63] = bf16(acc + shared sum), only inside [col_start, col_end).
+    auto emit = [&](int t, int hc, const float* v0, const float* v1, const float* sums) {
+      uint16_t* dst = p.out + static_cast<size_t>(t) * p.H + hc;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const int hh = hc + g * 8;
+        if (hh < p.col_start || hh >= p.col_end) continue;
+        const float* a = g < 4 ? &v0[g * 8] : &v1[(g - 4) * 8];
+        const float* b = &sums[g * 8];
+        uint4 o;
+        o.x = pack_bf16x2(a[0] + b[0], a[1] + b[1]);
+        o.y = pack_bf16x2(a[2] + b[2], a[3] + b[3]);
+        o.z = pack_bf16x2(a[4] + b[4], a[5] + b[5]);
+        o.w = pack_bf16x2(a[6] + b[6], a[7] + b[7]);
+        *reinterpret_cast<uint4*>(dst + g * 8) = o;
+      }
+    };
     int k = 0;
     bool alive = true;
     for (int i = 0; i < my_tiles && alive; ++i) {
@@ -339,6 +371,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!alive) break;
         }
+        if (p.stage_sums) {
+          // Single tile per pair: the second accumulator's columns are idle, so
+          // park this chunk's FP32 sums there and go on to the next chunk's
+          // partials without waiting for the MMAs; the sums are added below.
+          __syncwarp();  // tcgen05.st needs the whole warp converged
+          const uint32_t scol = tmem + lane_base + static_cast<uint32_t>(kTileH + ch * kChunk);
+          tmem_st32(scol, &s[0]);
+          tmem_st32(scol + 32u, &s[32]);
+          continue;
+        }
         if (!acc_ready) {
           bool ok = mbar_wait_cluster(smem_u32(&accf_bar[acc]), use & 1u, p.err, abort_v);
           ok = __all_sync(0xffffffffu, ok);
@@ -353,31 +395,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();  // tcgen05.ld needs the whole warp converged
         tmem_ld32(dcol + static_cast<uint32_t>(ch * kChunk), v0);
         tmem_ld32(dcol + static_cast<uint32_t>(ch * kChunk + 32), v1);
-        if (ch == kChunks - 1) {  // accumulator fully read: hand it back to the MMA issuer
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            const uint32_t bar = smem_u32(&acce_bar[acc]);
-            if (rank == 0)
-              mbar_arrive(bar);
-            else
-              mbar_arrive_remote(map_to_rank(bar, 0));
-          }
-        }
+        if (ch == kChunks - 1) release_acc(acc);
         if (!active || !row_ok) continue;
-        uint16_t* dst = p.out + static_cast<size_t>(t) * p.H + hc;
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const int hh = hc + g * 8;
-          if (hh < p.col_start || hh >= p.col_end) continue;
-          const float* a = g < 4 ? &v0[g * 8] : &v1[(g - 4) * 8];
-          const float* b = &s[g * 8];
-          uint4 o;
-          o.x = pack_bf16x2(a[0] + b[0], a[1] + b[1]);
-          o.y = pack_bf16x2(a[2] + b[2], a[3] + b[3]);
-          o.z = pack_bf16x2(a[4] + b[4], a[5] + b[5]);
-          o.w = pack_bf16x2(a[6] + b[6], a[7] + b[7]);
-          *reinterpret_cast<uint4*>(dst + g * 8) = o;
+        emit(t, hc, v0, v1, s);
+      }
+      if (p.stage_sums && alive) {
+        // The parked sums plus the accumulator, chunk by chunk.
+        tmem_wait_st();
+        bool ok = mbar_wait_cluster(smem_u32(&accf_bar[acc]), use & 1u, p.err, abort_v);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < kChunks; ++ch) {
+          const int hc = c.h0 + ch * kChunk;
+          const bool active = has_rows && chunk_active(p, hc);
+          float v0[32], v1[32], sums[kChunk];
+          __syncwarp();
+          tmem_ld32(dcol + static_cast<uint32_t>(ch * kChunk), v0);
+          tmem_ld32(dcol + static_cast<uint32_t>(ch * kChunk + 32), v1);
+          const uint32_t scol = tmem + lane_base + static_cast<uint32_t>(kTileH + ch * kChunk);
+          tmem_ld32(scol, *reinterpret_cast<float(*)[32]>(&sums[0]));
+          tmem_ld32(scol + 32u, *reinterpret_cast<float(*)[32]>(&sums[32]));
+          if (ch == kChunks - 1) release_acc(acc);
+          if (!active || !row_ok) continue;
+          emit(t, hc, v0, v1, sums);
         }
       }
     }
@@ -445,6 +490,11 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   p.pdl = a.pdl ? 1 : 0;
   p.err = dev.err_word;
   const long long tiles = static_cast<long long>(p.n_htiles) * p.n_tpairs;
+  p.stage_sums = tiles <= dev.num_sms / 2 ? 1 : 0;  // one tile per pair at most
+#ifdef LT_TUNING
+  p.stage_sums = env_int("LT_PREFILL_STAGE_SUMS", p.stage_sums);
+  if (tiles > dev.num_sms / 2) p.stage_sums = 0;
+#endif
   const int grid = 2 * static_cast<int>(std::min<long long>(dev.num_sms / 2, tiles));
 
   // The shared partials as one 2-D tensor [P*T rows, H columns]: the box for

@@ -77,3 +77,18 @@ def test_stress_sixteen_shards_full_size():
                                          ws)
     binding.latent_tail_check()
     assert torch.equal(stitched.view(torch.int16), full.view(torch.int16))
+
+
+def test_single_tile_and_multi_tile_epilogues_agree_bitwise():
+    """T = 600, H = 7168: the full call has 84 tiles for 76 CTA pairs (two tiles for
+    some pairs: accumulators double-buffered), each 1792-column shard has 21 tiles (one
+    per pair: the shared sums are parked in the idle accumulator's TMEM columns while
+    the mainloop runs). Both must give the same bits."""
+    P, T, L, H = 8, 600, 2048, 7168
+    x = gh.to_dev(inputs.make(P, T, L, H, seed=6007))
+    full = gh.run(x)
+    stitched = sentinel_out(T, H)
+    for k in range(4):
+        c0, c1 = k * 1792, (k + 1) * 1792
+        gh.run(x, c0, c1, out=stitched)
+    assert torch.equal(stitched.view(torch.int16), full.view(torch.int16))
