@@ -41,17 +41,18 @@ namespace lt {
 namespace {
 
 constexpr int kTileT = 128;   // tokens per CTA (half of the pair's MMA M = 256)
-constexpr int kTileH = 256;   // output columns per tile (MMA N)
-constexpr int kHalfH = kTileH / 2;  // W rows loaded by each CTA of the pair
+constexpr int kTileH = 256;   // output columns per tile (MMA N), T > 256
+constexpr int kNarrowTileH = 128;  // T <= 256: twice the tiles, so twice the pairs busy
 constexpr int kBlockK = 64;
 constexpr int kMaxStages = 6;
 constexpr int kChunk = 64;    // output columns per shared-partial box
-constexpr int kChunks = kTileH / kChunk;
 constexpr int kMaxSlots = 8;  // shared-partial ring depth limit
 constexpr int kThreads = 224;
 constexpr uint32_t kAStage = kTileT * kBlockK * 2;  // 16 KB of y
-constexpr uint32_t kBStage = kHalfH * kBlockK * 2;  // 16 KB of W (this CTA's half)
-constexpr uint32_t kStageBytes = kAStage + kBStage;
+// Stage = y [128 x 64] then this CTA's half of the W tile [tile_h/2 x 64].
+constexpr uint32_t stage_bytes_for(int tile_h) {
+  return kAStage + static_cast<uint32_t>(tile_h / 2) * kBlockK * 2;
+}
 constexpr uint32_t kSlotBytes = kTileT * kChunk * 2;  // 16 KB
 constexpr uint32_t kTmemCols = 2 * kTileH;
 constexpr size_t kSmemLimit = 226 * 1024;  // + static shared memory <= opt-in maximum
@@ -67,15 +68,17 @@ constexpr int kDefaultSlots = 5;
 constexpr int kSinglePartialStages = 6;
 constexpr int kSinglePartialSlots = 2;
 
-size_t smem_bytes(int stages, int slots) {
-  return 1024 + static_cast<size_t>(stages) * kStageBytes + static_cast<size_t>(slots) * kSlotBytes;
+size_t smem_bytes(int stages, int slots, int tile_h) {
+  return 1024 + static_cast<size_t>(stages) * stage_bytes_for(tile_h) +
+         static_cast<size_t>(slots) * kSlotBytes;
 }
 
 struct PrefillParams {
   uint16_t* out;
   int P, T, L, H;
   int col_start, col_end;
-  int htile0;       // absolute index of the first 256-column tile
+  int tile_h;       // output columns per tile: kTileH or kNarrowTileH
+  int htile0;       // absolute index of the first tile_h-column tile
   int n_htiles;
   int n_tpairs;     // 256-token groups (one per CTA pair and tile)
   int total_kb;
@@ -103,7 +106,7 @@ struct TileCoord {
 __device__ __forceinline__ TileCoord tile_coord(const PrefillParams& p, int tile, int rank) {
   TileCoord c;
   c.t0 = (tile / p.n_htiles) * (2 * kTileT) + rank * kTileT;
-  c.h0 = (p.htile0 + tile % p.n_htiles) * kTileH;
+  c.h0 = (p.htile0 + tile % p.n_htiles) * p.tile_h;
   return c;
 }
 
@@ -146,8 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
   const int n_stages = p.stages;
+  const int tile_h = p.tile_h;
+  const int half_h = tile_h / 2;        // W rows loaded by each CTA of the pair
+  const int n_chunks = tile_h / kChunk;
+  const uint32_t stage_bytes = stage_bytes_for(tile_h);
   const int n_slots = p.slots;
-  const uint32_t slot_base = sbase + static_cast<uint32_t>(n_stages) * kStageBytes;
+  const uint32_t slot_base = sbase + static_cast<uint32_t>(n_stages) * stage_bytes;
   const uint8_t* slot_gen = smem_raw + (slot_base - raw_u32);
   const int num_tiles = p.n_tpairs * p.n_htiles;
   const int my_tiles = pair < num_tiles ? (num_tiles - 1 - pair) / n_pairs + 1 : 0;
@@ -197,17 +204,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         TileCoord c;
         int kb;
         coord_of(it, c, kb);
-        const uint32_t st = sbase + static_cast<uint32_t>(it) * kStageBytes;
-        if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[it]), 2 * kStageBytes);
+        const uint32_t st = sbase + static_cast<uint32_t>(it) * stage_bytes;
+        if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[it]), 2 * stage_bytes);
         tma_load_2d_pair_hint(st + kAStage, &w_map, full_of(it), kb * kBlockK,
-                              c.h0 + rank * kHalfH, keep);
+                              c.h0 + rank * half_h, keep);
       }
       if (p.pdl) pdl_wait();
       for (int it = 0; it < pre; ++it) {
         TileCoord c;
         int kb;
         coord_of(it, c, kb);
-        const uint32_t st = sbase + static_cast<uint32_t>(it) * kStageBytes;
+        const uint32_t st = sbase + static_cast<uint32_t>(it) * stage_bytes;
         tma_load_2d_pair_hint(st, &y_map, full_of(it), kb * kBlockK, c.t0, keep);
       }
       int issued = pre;
@@ -218,10 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         TileCoord c;
         int kb;
         coord_of(it, c, kb);
-        const uint32_t st = sbase + static_cast<uint32_t>(s) * kStageBytes;
-        if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * kStageBytes);
+        const uint32_t st = sbase + static_cast<uint32_t>(s) * stage_bytes;
+        if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * stage_bytes);
         tma_load_2d_pair_hint(st, &y_map, full_of(s), kb * kBlockK, c.t0, keep);
-        tma_load_2d_pair_hint(st + kAStage, &w_map, full_of(s), kb * kBlockK, c.h0 + rank * kHalfH,
+        tma_load_2d_pair_hint(st + kAStage, &w_map, full_of(s), kb * kBlockK, c.h0 + rank * half_h,
                               keep);
         issued = it + 1;
       }
@@ -235,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && my_tiles > 0) {
       if (rank == 0) {
         // ---------------- pair MMA issuer ----------------
-        const uint32_t idesc = umma_idesc_bf16(2 * kTileT, kTileH);
+        const uint32_t idesc = umma_idesc_bf16(2 * kTileT, tile_h);
         int it = 0;
         bool alive = true;
         for (int i = 0; i < my_tiles && alive; ++i) {
@@ -243,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t use = static_cast<uint32_t>(i >> 1);
           if (!mbar_wait_cluster(smem_u32(&acce_bar[acc]), (use & 1u) ^ 1u, p.err, abort_v)) break;
           tc_fence_after();
-          const uint32_t d = tmem + static_cast<uint32_t>(acc * kTileH);
+          const uint32_t d = tmem + static_cast<uint32_t>(acc * tile_h);
           for (int kb = 0; kb < p.total_kb; ++kb, ++it) {
             const int s = it % n_stages;
             const uint32_t round = static_cast<uint32_t>(it / n_stages);
@@ -252,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a = sbase + static_cast<uint32_t>(s) * kStageBytes;
+            const uint32_t a = sbase + static_cast<uint32_t>(s) * stage_bytes;
             const uint32_t b = a + kAStage;
 #pragma unroll
             for (int k = 0; k < kBlockK / 16; ++k)
@@ -274,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < my_tiles && alive; ++i) {
         const TileCoord c = tile_coord(p, pair + i * n_pairs, rank);
         if (c.t0 >= p.T) continue;  // no rows of this CTA in the tile
-        for (int ch = 0; ch < kChunks && alive; ++ch) {
+        for (int ch = 0; ch < n_chunks && alive; ++ch) {
           const int hc = c.h0 + ch * kChunk;
           if (!chunk_active(p, hc)) continue;
           for (int pp = 0; pp < p.P; ++pp, ++k) {
@@ -340,10 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = c.t0 + r;
       const bool row_ok = t < p.T;
       const bool has_rows = c.t0 < p.T;
-      const uint32_t dcol = tmem + lane_base + static_cast<uint32_t>(acc * kTileH);
+      const uint32_t dcol = tmem + lane_base + static_cast<uint32_t>(acc * tile_h);
       bool acc_ready = false;
 #pragma unroll 1
-      for (int ch = 0; ch < kChunks; ++ch) {
+      for (int ch = 0; ch < n_chunks; ++ch) {
         const int hc = c.h0 + ch * kChunk;
         const bool active = has_rows && chunk_active(p, hc);
         float s[kChunk];
@@ -376,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // park this chunk's FP32 sums there and go on to the next chunk's
           // partials without waiting for the MMAs; the sums are added below.
           __syncwarp();  // tcgen05.st needs the whole warp converged
-          const uint32_t scol = tmem + lane_base + static_cast<uint32_t>(kTileH + ch * kChunk);
+          const uint32_t scol = tmem + lane_base + static_cast<uint32_t>(tile_h + ch * kChunk);
           tmem_st32(scol, &s[0]);
           tmem_st32(scol + 32u, &s[32]);
           continue;
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();  // tcgen05.ld needs the whole warp converged
         tmem_ld32(dcol + static_cast<uint32_t>(ch * kChunk), v0);
         tmem_ld32(dcol + static_cast<uint32_t>(ch * kChunk + 32), v1);
-        if (ch == kChunks - 1) release_acc(acc);
+        if (ch == n_chunks - 1) release_acc(acc);
         if (!active || !row_ok) continue;
         emit(t, hc, v0, v1, s);
       }
@@ -410,17 +417,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 #pragma unroll 1
-        for (int ch = 0; ch < kChunks; ++ch) {
+        for (int ch = 0; ch < n_chunks; ++ch) {
           const int hc = c.h0 + ch * kChunk;
           const bool active = has_rows && chunk_active(p, hc);
           float v0[32], v1[32], sums[kChunk];
           __syncwarp();
           tmem_ld32(dcol + static_cast<uint32_t>(ch * kChunk), v0);
           tmem_ld32(dcol + static_cast<uint32_t>(ch * kChunk + 32), v1);
-          const uint32_t scol = tmem + lane_base + static_cast<uint32_t>(kTileH + ch * kChunk);
+          const uint32_t scol = tmem + lane_base + static_cast<uint32_t>(tile_h + ch * kChunk);
           tmem_ld32(scol, *reinterpret_cast<float(*)[32]>(&sums[0]));
           tmem_ld32(scol + 32u, *reinterpret_cast<float(*)[32]>(&sums[32]));
-          if (ch == kChunks - 1) release_acc(acc);
+          if (ch == n_chunks - 1) release_acc(acc);
           if (!active || !row_ok) continue;
           emit(t, hc, v0, v1, sums);
         }
@@ -471,8 +478,14 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   p.H = a.H;
   p.col_start = a.col_start;
   p.col_end = a.col_end;
-  p.htile0 = a.col_start / kTileH;
-  p.n_htiles = (a.col_end - 1) / kTileH - p.htile0 + 1;
+  // A fixed function of T (never of the column range), so that every output
+  // element is computed the same way whatever range a call asks for.
+  p.tile_h = a.T <= 2 * kTileT ? kNarrowTileH : kTileH;
+#ifdef LT_TUNING
+  p.tile_h = env_int("LT_PREFILL_TILE_H", p.tile_h) == kNarrowTileH ? kNarrowTileH : kTileH;
+#endif
+  p.htile0 = a.col_start / p.tile_h;
+  p.n_htiles = (a.col_end - 1) / p.tile_h - p.htile0 + 1;
   p.n_tpairs = ceil_div(a.T, 2 * kTileT);
   p.total_kb = ceil_div(a.L, kBlockK);
   p.stages = kDefaultStages;
@@ -480,12 +493,14 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   if (a.P == 1) {  // one box per chunk: the operand ring gets the bytes (measured)
     p.stages = kSinglePartialStages;
     p.slots = kSinglePartialSlots;
+  } else if (p.tile_h == kNarrowTileH) {  // 24 KB stages: two more fit beside the slots
+    p.stages = kMaxStages;
   }
 #ifdef LT_TUNING
   p.stages = std::min(std::max(1, env_int("LT_PREFILL_STAGES", p.stages)), kMaxStages);
   p.slots = std::min(std::max(1, env_int("LT_PREFILL_SLOTS", p.slots)), kMaxSlots);
 #endif
-  const size_t smem = smem_bytes(p.stages, p.slots);
+  const size_t smem = smem_bytes(p.stages, p.slots, p.tile_h);
   if (smem > kSmemLimit) return cudaErrorInvalidConfiguration;
   p.pdl = a.pdl ? 1 : 0;
   p.err = dev.err_word;
@@ -503,7 +518,8 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   // and columns past H read as zero.
   CUtensorMap y_map, w_map, s_map;
   if (!make_map_bf16_sw128(&y_map, a.y, a.T, a.L, kTileT)) return cudaErrorInvalidValue;
-  if (!make_map_bf16_sw128(&w_map, a.W, a.H, a.L, kHalfH)) return cudaErrorInvalidValue;
+  if (!make_map_bf16_sw128(&w_map, a.W, a.H, a.L, static_cast<uint32_t>(p.tile_h / 2)))
+    return cudaErrorInvalidValue;
   if (!make_map_bf16_sw128(&s_map, a.shared, static_cast<uint64_t>(a.P) * a.T, a.H, kTileT))
     return cudaErrorInvalidValue;
 
