@@ -103,10 +103,11 @@ struct TileCoord {
 };
 
 // Pair tile `tile` -> coordinates for the CTA of rank `rank` in the pair.
+template <int kTileW>
 __device__ __forceinline__ TileCoord tile_coord(const PrefillParams& p, int tile, int rank) {
   TileCoord c;
   c.t0 = (tile / p.n_htiles) * (2 * kTileT) + rank * kTileT;
-  c.h0 = (p.htile0 + tile % p.n_htiles) * p.tile_h;
+  c.h0 = (p.htile0 + tile % p.n_htiles) * kTileW;
   return c;
 }
 
@@ -127,6 +128,9 @@ __device__ __forceinline__ void add8(float* s, const uint4& v) {
   s[7] += bf16_hi(v.w);
 }
 
+// kTileW: output columns per tile (MMA N), a compile-time constant so that the
+// issue loops keep their address arithmetic constant.
+template <int kTileW>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap y_map,
                    const __grid_constant__ CUtensorMap w_map,
@@ -149,10 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
   const int n_stages = p.stages;
-  const int tile_h = p.tile_h;
-  const int half_h = tile_h / 2;        // W rows loaded by each CTA of the pair
-  const int n_chunks = tile_h / kChunk;
-  const uint32_t stage_bytes = stage_bytes_for(tile_h);
+  constexpr int tile_h = kTileW;
+  constexpr int half_h = tile_h / 2;        // W rows loaded by each CTA of the pair
+  constexpr int n_chunks = tile_h / kChunk;
+  constexpr uint32_t stage_bytes = stage_bytes_for(tile_h);
   const int n_slots = p.slots;
   const uint32_t slot_base = sbase + static_cast<uint32_t>(n_stages) * stage_bytes;
   const uint8_t* slot_gen = smem_raw + (slot_base - raw_u32);
@@ -197,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto coord_of = [&](int it, TileCoord& c, int& kb) {
         const int local = it / p.total_kb;
         kb = it - local * p.total_kb;
-        c = tile_coord(p, pair + local * n_pairs, rank);
+        c = tile_coord<kTileW>(p, pair + local * n_pairs, rank);
       };
       auto full_of = [&](int s) { return map_to_rank(smem_u32(&full_bar[s]), 0); };
       for (int it = 0; it < pre; ++it) {  // W does not depend on the norm kernel
@@ -279,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int k = 0;
       bool alive = true;
       for (int i = 0; i < my_tiles && alive; ++i) {
-        const TileCoord c = tile_coord(p, pair + i * n_pairs, rank);
+        const TileCoord c = tile_coord<kTileW>(p, pair + i * n_pairs, rank);
         if (c.t0 >= p.T) continue;  // no rows of this CTA in the tile
         for (int ch = 0; ch < n_chunks && alive; ++ch) {
           const int hc = c.h0 + ch * kChunk;
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < my_tiles && alive; ++i) {
       const int acc = i & 1;
       const uint32_t use = static_cast<uint32_t>(i >> 1);
-      const TileCoord c = tile_coord(p, pair + i * n_pairs, rank);
+      const TileCoord c = tile_coord<kTileW>(p, pair + i * n_pairs, rank);
       const int t = c.t0 + r;
       const bool row_ok = t < p.T;
       const bool has_rows = c.t0 < p.T;
@@ -465,7 +469,12 @@ int env_int(const char* name, int dflt) {
 }  // namespace
 
 cudaError_t setup_prefill(const DeviceInfo&) {
-  return cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kTileH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemLimit));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prefill_kernel<kNarrowTileH>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(kSmemLimit));
 }
 
@@ -542,7 +551,9 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   }
   cfg.attrs = attrs;
   cfg.numAttrs = static_cast<unsigned>(n);
-  return cudaLaunchKernelEx(&cfg, prefill_kernel, y_map, w_map, s_map, p);
+  if (p.tile_h == kNarrowTileH)
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<kNarrowTileH>, y_map, w_map, s_map, p);
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<kTileH>, y_map, w_map, s_map, p);
 }
 
 }  // namespace lt
