@@ -9,16 +9,19 @@
 // the tensor-core mainloop, fed from L2 (y and W are re-read per tile), and
 // the HBM stream of shared partials, fed by TMA independently of the MMAs.
 //
-// Each SM can take in only about 120 GB/s from L2 through TMA, so the bytes a
-// CTA must ingest per tile bound the kernel. Pairs of CTAs (a 2-CTA cluster)
-// therefore share one tensor-core product (tcgen05 cta_group::2, M = 256
-// tokens, N = 256 columns): each CTA loads its own 128 tokens of y and half of
-// the W tile, which halves the operand bytes per CTA.
+// What one SM can take in per unit time (bytes in flight over the L2 / HBM
+// round trip) bounds the kernel, so the bytes a CTA must ingest per tile
+// matter. Pairs of CTAs (a 2-CTA cluster) therefore share one tensor-core
+// product (tcgen05 cta_group::2, M = 256 tokens, N = tile width): each CTA loads
+// its own 128 tokens of y and half of the W tile, which halves the operand bytes
+// per CTA. The tile width is 256 columns, or 128 for T <= 256 so that the few
+// tiles of a short call still occupy twice the CTA pairs (a template parameter,
+// chosen from T alone).
 //
 // Persistent, warp-specialized kernel, one CTA per SM, 7 warps per CTA:
-//   warp 0      operand producer: y [128 tokens x 64] and W [128 rows x 64] per
-//               K-block into this CTA's stage ring (128B swizzle, L2 evict-last:
-//               every operand tile is read by many CTAs);
+//   warp 0      operand producer: y [128 tokens x 64] and W [width/2 rows x 64]
+//               per K-block into this CTA's stage ring (128B swizzle, L2
+//               evict-last: every operand tile is read by many CTAs);
 //   warp 1      TMEM allocation for the pair; in the even CTA the single-thread
 //               MMA issuer (both CTAs' TMA copies of a stage complete on the even
 //               CTA's barrier; its commits arrive on the stage and accumulator
@@ -28,10 +31,14 @@
 //               ring (L2 evict-first: read once);
 //   warps 2..5  epilogue, one token row per thread: sum the P partial boxes of
 //               a chunk in FP32 (p ascending), add the accumulator columns from
-//               this CTA's TMEM (two 256-column accumulators), round to bf16 and
-//               store 16-byte vectors.
-// Output tiles sit at absolute multiples of 256 columns, so a column-range call
-// computes each element exactly as the full call does.
+//               this CTA's TMEM (two accumulators, so the next tile's MMAs run
+//               during this tile's epilogue), round to bf16 and store 16-byte
+//               vectors. When every pair owns a single tile there is no next
+//               tile to overlap: the epilogue then parks each chunk's FP32 sums
+//               in the idle second accumulator's TMEM columns while the MMAs
+//               run, and adds them to the accumulator afterwards (same bits).
+// Output tiles sit at absolute multiples of the tile width, so a column-range
+// call computes each element exactly as the full call does.
 #include "launch.h"
 #include "ptx.cuh"
 
