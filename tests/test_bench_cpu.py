@@ -1,0 +1,70 @@
+"""bench.py's host-side arithmetic and bookkeeping (no GPU): the algorithmic byte
+and flop counts the roofline divides by, the whole-job throughput, and the rule
+that a profiled DRAM traffic figure is reported only while the kernel's source is
+the one that was captured."""
+
+import hashlib
+import importlib
+import sys
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+sys.path.insert(0, str(ROOT))
+bench = importlib.import_module("bench")
+
+
+@pytest.mark.parametrize("P,T,width,mb,gflop", [
+    # bytes = P*T*L*2 (routed) + P*T*w*2 (shared) + w*L*2 (W) + T*w*2 (out) + L*4 (g)
+    (8, 1, 7168, 29.53, 0.02936),
+    (8, 16, 7168, 31.96, 0.470),
+    (8, 128, 7168, 50.08, 3.758),
+    (8, 8192, 7168, 1354.8, 240.5),
+    (16, 16384, 7168, 5096.1, 481.0),
+    (16, 16384, 448, 1325.1, 30.1),   # one of the 16 stress column shards
+    (1, 8192, 7168, 297.8, 240.5),    # pre-reduced P = 1 workload
+])
+def test_algorithmic_bytes_and_flops(P, T, width, mb, gflop):
+    L = 2048
+    assert bench.call_bytes(P, T, L, width) / 1e6 == pytest.approx(mb, abs=0.06)
+    assert bench.flops(T, L, width) / 1e9 == pytest.approx(gflop, rel=2e-3)
+
+
+def test_projection_bytes_exclude_the_routed_partials():
+    P, T, L, w = 8, 16, 2048, 7168
+    # the projection reads the latent y (T*L*2) instead of the P routed partials
+    assert bench.call_bytes(P, T, L, w) - bench.project_bytes(P, T, L, w) == \
+        P * T * L * 2 - T * L * 2 + L * 4
+
+
+def test_job_throughput_counts_every_rank_over_the_slowest_time():
+    assert bench.job_throughput(16, 1000, 4, 0.01) == pytest.approx(16 * 1000 * 4 / 0.01)
+
+
+def _write_profile(dirpath, kernel, digest, workload="decode", T=16, nbytes=31292160):
+    (dirpath / f"{kernel}_X.md").write_text(
+        f"# summary\n\ntraffic_per_launch_bytes: {nbytes} (workload {workload}, T {T}, "
+        f"{kernel.replace('_kernel', '')}.cu sha256 {digest})\n")
+
+
+def test_profiled_traffic_needs_matching_workload_and_source(tmp_path, monkeypatch):
+    csrc = tmp_path / "latent_moe_output_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    src = csrc / "decode.cu"
+    src.write_text("// kernel source as captured\n")
+    digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    _write_profile(tmp_path / "profiles", "decode_kernel", digest)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("decode_kernel", "decode", 16) == 31292160
+    assert bench.profiled_traffic("decode_kernel", "decode", 8) is None        # other T
+    assert bench.profiled_traffic("decode_kernel", "prefill", 16) is None      # other workload
+    src.write_text("// kernel source changed since the capture\n")
+    assert bench.profiled_traffic("decode_kernel", "decode", 16) is None       # stale capture
+
+
+def test_committed_decode_capture_matches_the_current_kernel():
+    """The repository's own decode summary must still describe decode.cu as built;
+    re-capture it (profiles/) whenever the kernel changes."""
+    assert bench.profiled_traffic("decode_kernel", "decode", 16) is not None
