@@ -190,7 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue warps 2..5 ----------------
     // (a) While W streams in: sum the P shared partials of this CTA's rows,
-    //     p ascending in FP32, into shared memory. Independent of the norm kernel.
+    //     p ascending in FP32, into shared memory. Independent of the norm kernel:
+    //     the work that wrote the partials finished before this kernel launched
+    //     (the norm kernel waited for it before releasing this one), so they are
+    //     read from L2 without waiting, never through a possibly stale L1.
     const int et = threadIdx.x - 64;
     const size_t plane = static_cast<size_t>(p.T) * p.H;
     const int items = p.T * groups;
@@ -205,11 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (; pp + 8 <= p.P; pp += 8) {
           uint4 v[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) v[k] = ld_stream_v4(src + (pp + k) * plane);
+          for (int k = 0; k < 8; ++k) v[k] = ld_l2_v4(src + (pp + k) * plane);
 #pragma unroll
           for (int k = 0; k < 8; ++k) add8(a, v[k]);
         }
-        for (; pp < p.P; ++pp) add8(a, ld_stream_v4(src + pp * plane));
+        for (; pp < p.P; ++pp) add8(a, ld_l2_v4(src + pp * plane));
       }
       float4* dst = reinterpret_cast<float4*>(ssum + t * rpc + g * 8);
       dst[0] = make_float4(a[0], a[1], a[2], a[3]);

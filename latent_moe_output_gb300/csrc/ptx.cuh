@@ -374,6 +374,17 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 
 // ------------------------------------------------------------ global I/O
+// 16-byte load served by L2 only (never from an SM's L1): for data written by
+// work that finished before this kernel launched but that this thread did not
+// itself wait for (griddepcontrol.wait); L2 is coherent for every writer.
+__device__ __forceinline__ uint4 ld_l2_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
