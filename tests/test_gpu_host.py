@@ -124,3 +124,44 @@ def test_host_rejects_pageable_and_device_memory():
         binding.latent_tail_forward_host(x.routed, hs, x.g, x.W, out, x.eps, ws)
     with pytest.raises(LatentTailError):
         binding.latent_tail_forward_host(x.routed.cpu(), hs, x.g, x.W, out, x.eps, ws)
+
+
+def test_host_memory_registered_with_cuda_host_register():
+    """Ordinary host buffers registered (mapped) with cudaHostRegister, not allocated
+    pinned, are accepted and give the device call's bits."""
+    import numpy as np
+
+    cudart = torch.cuda.cudart()
+    if not hasattr(cudart, "cudaHostRegister"):
+        pytest.skip("this torch build does not expose cudaHostRegister")
+    P, T, L, H = 4, 16, 1024, 2048
+    x = inputs.make(P, T, L, H, seed=7500, device="cuda")
+    keep, registered = [], []
+
+    def registered_like(shape, src=None):
+        n = int(np.prod(shape)) * 2
+        raw = np.empty(n + 8192, dtype=np.uint8)
+        off = (-raw.ctypes.data) % 4096
+        t = torch.from_numpy(raw[off:off + n]).view(torch.bfloat16).view(*shape)
+        if src is not None:
+            t.copy_(src.cpu())
+        rc = cudart.cudaHostRegister(t.data_ptr(), n, 2)  # cudaHostRegisterMapped
+        assert int(rc) == 0, f"cudaHostRegister failed: {rc}"
+        keep.append(raw)
+        registered.append(t.data_ptr())
+        return t
+
+    try:
+        hr = registered_like((P, T, L), x.routed)
+        hs = registered_like((P, T, H), x.shared)
+        out = registered_like((T, H))
+        ws = torch.empty(binding.latent_tail_host_workspace_size(P, T, L, H), dtype=torch.uint8,
+                         device="cuda")
+        binding.latent_tail_forward_host(hr, hs, x.g, x.W, out, x.eps, ws)
+        torch.cuda.synchronize()
+        binding.latent_tail_check()
+        assert torch.equal(out, _device_result(x, x.g))
+    finally:
+        torch.cuda.synchronize()
+        for ptr in registered:
+            cudart.cudaHostUnregister(ptr)
