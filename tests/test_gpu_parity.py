@@ -51,6 +51,12 @@ def test_decode_sweep(w):
     (4, 520, 2048, 512),   # several token tiles at the production latent width
     (1, 1000, 64, 2056),   # many tiles, one K-block, P = 1 (pre-reduced latent)
     (16, 200, 256, 264),   # P = 16 partials
+    (64, 4, 256, 256),     # P = 64, the largest partial count accepted (decode)
+    (64, 200, 128, 256),   # P = 64 on the prefill path
+    (2, 8, 16384, 256),    # L = 16384, the largest latent width accepted (decode)
+    (2, 260, 16384, 128),  # L = 16384 on the prefill path
+    (1, 3, 8, 8),          # L = H = 8, the smallest accepted: boxes wider than the tensor
+    (2, 130, 8, 16),       # the same on the prefill path
 ])
 def test_ragged_shapes(P, T, L, H):
     x = inputs.make(P, T, L, H, seed=P * 1000 + T)
