@@ -42,7 +42,7 @@ def test_overlapping_output_is_rejected():
 
 
 @pytest.mark.parametrize("T,c0,c1", [(16, 0, 1024), (16, 256, 512), (300, 0, 1024),
-                                     (300, 128, 896)])
+                                     (300, 128, 896), (200, 0, 1024), (200, 128, 896)])
 def test_in_place_into_a_shared_partial(T, c0, c1):
     """out aliasing shared[p] (the pages' in-place addmm_ into the shared
     output): same values as the out-of-place call; columns outside the range

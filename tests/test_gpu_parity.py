@@ -117,7 +117,8 @@ def test_zero_tokens():
     binding.latent_tail_check()
 
 
-@pytest.mark.parametrize("P,T,L,H", [(2, 5, 64, 128), (8, 16, 2048, 7168), (3, 300, 328, 1000)])
+@pytest.mark.parametrize("P,T,L,H", [(2, 5, 64, 128), (8, 16, 2048, 7168), (3, 300, 328, 1000),
+                                     (2, 200, 256, 1000)])
 def test_no_norm_branch(P, T, L, H):
     """norm_weight = None: the latent is the routed partial sum itself (the
     `transform.norm is None` branch of `_shard_up_proj_tail`)."""
