@@ -426,13 +426,26 @@ def ours(args):
                 binding.latent_tail_forward_cols(x.routed, x.shared, x.g, x.W, out, x.eps,
                                                  bounds[k], bounds[k + 1], ws, stream)
 
+        # The same shards with the latent computed once per step: one norm call,
+        # then N projection calls over [0, H).
+        def shard_step_norm_once(i):
+            x, out, ws = sets[i % n_sets]
+            y = ws[:T * L * 2].view(torch.bfloat16).view(T, L)
+            binding.latent_tail_norm(x.routed, x.g, y, x.eps, stream)
+            for k in range(args.shards):
+                binding.latent_tail_project_cols(y, x.shared, x.W, out, bounds[k], bounds[k + 1],
+                                                 stream)
+
         shard_steps = max(1, min(args.steps, 20))
         t_shards = max_over_ranks(timed(shard_step, shard_steps), world)
+        t_once = max_over_ranks(timed(shard_step_norm_once, shard_steps), world)
         binding.latent_tail_check(stream)
         shard_line = {"calls_per_step": args.shards, "steps": shard_steps,
                       "us_per_step": round(t_shards / shard_steps * 1e6, 3),
                       "tokens_per_s": round(job_throughput(T, shard_steps, world, t_shards), 1),
-                      "note": "each call reduces and normalizes all T tokens again"}
+                      "note": "each call reduces and normalizes all T tokens again",
+                      "norm_once_us_per_step": round(t_once / shard_steps * 1e6, 3),
+                      "norm_once_note": "latent_tail_norm once, then N latent_tail_project_cols"}
 
     # One call at a time, with nothing before or after it on the GPU (no overlap
     # with a neighbouring call): a spin kernel keeps the GPU busy while the
