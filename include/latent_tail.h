@@ -100,9 +100,11 @@ LT_API size_t latent_tail_workspace_size(int P, int T, int L, int H);
  * Launches two kernels: reduce + RMSNorm into the workspace, then the
  * up-projection with the shared-partial epilogue (decode kernel for T <= 128,
  * persistent tensor-core kernel above), chained by programmatic dependent
- * launch. For T <= 128 the first kernel also prefetches the W rows into L2
- * before it waits for the preceding work on the stream (W is only read).
- * Capturable in a CUDA graph.
+ * launch. For T <= 128 the first kernel also prefetches routed and the W rows
+ * into L2 before it waits for the preceding work on the stream (an L2
+ * prefetch is only a hint: if that work is still writing routed, the lines are
+ * updated in L2 and every read happens after the wait). Calls issued back to
+ * back on one stream may share one workspace. Capturable in a CUDA graph.
  */
 LT_API lt_status latent_tail_forward(const uint16_t* routed, const uint16_t* shared,
                                      const float* norm_weight, const uint16_t* W,
