@@ -68,3 +68,38 @@ def test_committed_decode_capture_matches_the_current_kernel():
     """The repository's own decode summary must still describe decode.cu as built;
     re-capture it (profiles/) whenever the kernel changes."""
     assert bench.profiled_traffic("decode_kernel", "decode", 16) is not None
+
+
+def test_workloads_are_the_benchmark_configurations():
+    from latent_moe_output_gb300 import inputs
+
+    w = inputs.WORKLOADS
+    assert (w["tiny"].P, w["tiny"].T, w["tiny"].L, w["tiny"].H, w["tiny"].seed) == (2, 5, 64, 128, 0)
+    assert (w["decode"].P, w["decode"].T, w["decode"].L, w["decode"].H) == (8, 16, 2048, 7168)
+    assert sorted(x.T for x in inputs.DECODE_SWEEP) == [1, 8, 32, 64, 128]
+    assert all(x.seed == 1000 + x.T and x.P == 8 for x in inputs.DECODE_SWEEP)
+    assert (w["prefill"].P, w["prefill"].T) == (8, 8192)
+    assert (w["stress"].P, w["stress"].T, w["stress"].outlier_rows) == (16, 16384, True)
+    assert inputs.STRESS_SHARDS == 16 and w["stress"].H % inputs.STRESS_SHARDS == 0
+    assert inputs.EPS == 1e-6
+
+
+def test_reference_arm_prints_one_complete_line(capsys, monkeypatch):
+    """`bench.py --impl reference` times the oracle and prints the contract's keys,
+    on rank 0 only."""
+    import json
+    import types
+
+    args = types.SimpleNamespace(workload="tiny", steps=2, warmup=1, gpus=1)
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    bench.reference_arm(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    monkeypatch.setenv("RANK", "1")
+    bench.reference_arm(args)
+    assert capsys.readouterr().out.strip() == ""
