@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         o.y = pack_bf16x2(a[2] + b[2], a[3] + b[3]);
         o.z = pack_bf16x2(a[4] + b[4], a[5] + b[5]);
         o.w = pack_bf16x2(a[6] + b[6], a[7] + b[7]);
-        *reinterpret_cast<uint4*>(dst + g * 8) = o;
+        st_stream_v4(dst + g * 8, o);
       }
     };
     int k = 0;

@@ -385,6 +385,14 @@ __device__ __forceinline__ uint4 ld_l2_v4(const void* p) {
   return v;
 }
 
+// 16-byte store marked streaming (evict first): output that is written once and
+// not read again by this kernel, so it does not displace re-read operands in L2.
+__device__ __forceinline__ void st_stream_v4(void* p, const uint4& v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
