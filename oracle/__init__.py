@@ -34,16 +34,18 @@ CXXFLAGS = ["-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math",
 _lib = None
 
 
-def build(out_path: Path | None = None, mutant: int = 0, force: bool = False) -> Path:
-    """Compile the oracle (optionally a planted-mistake mutant) and return the .so path."""
+def build(out_path: Path | None = None, source: Path | None = None,
+          force: bool = False) -> Path:
+    """Compile the oracle and return the .so path. ``source`` replaces the
+    oracle's own source file (the mutation test compiles patched copies)."""
     out = Path(out_path) if out_path is not None else LIB_PATH
-    if mutant == 0 and out_path is None and out.exists() and not force:
+    src = Path(source) if source is not None else SOURCE
+    if source is None and out_path is None and out.exists() and not force:
         if out.stat().st_mtime >= SOURCE.stat().st_mtime:
             return out
     out.parent.mkdir(parents=True, exist_ok=True)
     tmp = out.with_name(out.name + f".tmp{os.getpid()}")
-    cmd = ["g++", *CXXFLAGS, f"-DLT_ORACLE_MUTANT={int(mutant)}", str(SOURCE),
-           "-o", str(tmp)]
+    cmd = ["g++", *CXXFLAGS, str(src), "-o", str(tmp)]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -59,7 +61,6 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = [vp, vp, lg, lg, lg, dbl, vp]
         fn.restype = ctypes.c_int
-    lib.lt_oracle_mutant_id.restype = ctypes.c_int
     return lib
 
 

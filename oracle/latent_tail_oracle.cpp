@@ -40,18 +40,14 @@
 // Build: g++ -O2 -ffp-contract=off -shared -fPIC (no fast-math, no FMA
 // contraction, so x86 and Arm hosts give the same bits).
 //
-// LT_ORACLE_MUTANT (compile-time, default 0) plants one deliberate mistake so
-// the CPU tests can show that their pins catch it. Production builds of the
-// oracle never define it.
+// The oracle's own tests plant mistakes in a temporary copy of this file (a
+// text patch per mistake) to show that its pins catch each one; this file
+// itself holds only the definition.
 
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <vector>
-
-#ifndef LT_ORACLE_MUTANT
-#define LT_ORACLE_MUTANT 0
-#endif
 
 namespace {
 
@@ -79,54 +75,18 @@ void normalized_latent(const uint16_t* routed, const float* g, long P, long T,
                        long L, long t, Acc eps, Acc* x, Acc* y) {
   for (long l = 0; l < L; ++l) {
     Acc s = 0;
-#if LT_ORACLE_MUTANT == 5
-    // mistake: partials read as if laid out [T,P,L]
-    for (long p = 0; p < P; ++p) s += widen_bf16(routed[((t * P) + p) * L + l]);
-#else
     for (long p = 0; p < P; ++p) s += widen_bf16(routed[((p * T) + t) * L + l]);
-#endif
     x[l] = s;
   }
   if (g == nullptr) {  // no norm: the latent is the partial sum itself
-#if LT_ORACLE_MUTANT == 10
-    // mistake: the no-norm branch still normalizes (with unit weight)
-    Acc ss0 = 0;
-    for (long l = 0; l < L; ++l) ss0 += x[l] * x[l];
-    const Acc r0 = static_cast<Acc>(1) / std::sqrt(ss0 / static_cast<Acc>(L) + eps);
-    for (long l = 0; l < L; ++l) y[l] = x[l] * r0;
-#else
     for (long l = 0; l < L; ++l) y[l] = x[l];
-#endif
     return;
   }
   Acc ss = 0;
-#if LT_ORACLE_MUTANT == 9
-  // mistake: squares of the partials summed instead of the square of the sum
-  for (long l = 0; l < L; ++l)
-    for (long p = 0; p < P; ++p) {
-      Acc v = widen_bf16(routed[((p * T) + t) * L + l]);
-      ss += v * v;
-    }
-#else
   for (long l = 0; l < L; ++l) ss += x[l] * x[l];
-#endif
-#if LT_ORACLE_MUTANT == 2
-  Acc ms = ss;  // mistake: sum of squares, not the mean
-#else
-  Acc ms = ss / static_cast<Acc>(L);
-#endif
-#if LT_ORACLE_MUTANT == 1
-  Acc r = static_cast<Acc>(1) / (std::sqrt(ms) + eps);  // mistake: eps outside
-#else
-  Acc r = static_cast<Acc>(1) / std::sqrt(ms + eps);
-#endif
-  for (long l = 0; l < L; ++l) {
-#if LT_ORACLE_MUTANT == 6
-    y[l] = x[l] * r;  // mistake: norm weight dropped
-#else
-    y[l] = x[l] * r * static_cast<Acc>(g[l]);
-#endif
-  }
+  const Acc ms = ss / static_cast<Acc>(L);
+  const Acc r = static_cast<Acc>(1) / std::sqrt(ms + eps);
+  for (long l = 0; l < L; ++l) y[l] = x[l] * r * static_cast<Acc>(g[l]);
 }
 
 template <typename Acc>
@@ -142,26 +102,10 @@ int forward(const uint16_t* routed, const uint16_t* shared, const float* g,
     normalized_latent<Acc>(routed, g, P, T, L, t, e, x.data(), y.data());
     for (long h = c0; h < c1; ++h) {
       Acc acc = 0;
-#if LT_ORACLE_MUTANT == 3
-      // mistake: W read transposed, as if it were [L,H]
-      for (long l = 0; l < L; ++l) acc += y[l] * widen_bf16(W[l * H + h]);
-#elif LT_ORACLE_MUTANT == 8
-      // mistake: W row taken relative to the column range start
-      for (long l = 0; l < L; ++l) acc += y[l] * widen_bf16(W[(h - c0) * L + l]);
-#else
       for (long l = 0; l < L; ++l) acc += y[l] * widen_bf16(W[h * L + l]);
-#endif
       Acc s = 0;
-#if LT_ORACLE_MUTANT == 4
-      for (long p = 1; p < P; ++p)  // mistake: first shared partial dropped
-        s += widen_bf16(shared[((p * T) + t) * H + h]);
-#elif LT_ORACLE_MUTANT == 7
-      for (long p = 0; p < P; ++p)  // mistake: shared read as [T,P,H]
-        s += widen_bf16(shared[((t * P) + p) * H + h]);
-#else
       for (long p = 0; p < P; ++p)
         s += widen_bf16(shared[((p * T) + t) * H + h]);
-#endif
       out[t * width + (h - c0)] = acc + s;
     }
   }
@@ -215,7 +159,5 @@ int lt_oracle_latent_f64(const uint16_t* routed, const float* g, long P, long T,
                          long L, double eps, double* y) {
   return latent<double>(routed, g, P, T, L, eps, y);
 }
-
-int lt_oracle_mutant_id(void) { return LT_ORACLE_MUTANT; }
 
 }  // extern "C"

@@ -21,6 +21,12 @@ test builds the oracle with planted mistakes and checks each one is caught):
 * no_norm           - without a norm weight the latent is the plain partial
                       sum: W = I gives out = sum_p routed + sum_p shared exactly,
                       and a permuted selection matrix picks x[t, pi(h)]
+* torch_formula     - the expectation the PR #51253 runner test prints,
+                      F.linear(F.rms_norm(sum_p routed, (L,), g, eps), W) + sum_p
+                      shared, evaluated by PyTorch's own CPU kernels in float64 on
+                      the tiny configuration and on decode shapes (P = 8, L = 2048,
+                      H = 7168, T = 1 and 16): the FP32 oracle agrees to FP32
+                      rounding, the double oracle to double rounding
 """
 
 from __future__ import annotations
@@ -221,5 +227,45 @@ def no_norm(lib):
         assert np.array_equal(y, x), f"no-norm latent ({prec})"
 
 
+def _formula(routed, shared, g, W, eps):
+    """The page test's expectation in float64: F.linear(F.rms_norm(all-reduced
+    routed, (L,), weight, eps), up_proj weight) plus the all-reduced shared
+    output, the all-reduce over ranks being the sum over the stacked partials.
+    Also returns sum_l |y W| + sum_p |shared|, the scale of the rounding error of
+    any evaluation order."""
+    import torch.nn.functional as F
+
+    L = routed.shape[-1]
+    x = routed.double().sum(0)
+    y = F.rms_norm(x, (L,), torch.as_tensor(g).double(), eps)
+    Wd = W.double()
+    out = F.linear(y, Wd) + shared.double().sum(0)
+    scale = F.linear(y.abs(), Wd.abs()) + shared.double().abs().sum(0)
+    return out.numpy(), scale.numpy()
+
+
+def torch_formula(lib):
+    from latent_moe_output_gb300 import inputs
+
+    cases = [inputs.make_workload(inputs.TINY),
+             inputs.make(8, 1, 2048, 7168, seed=21),
+             inputs.make(8, 16, 2048, 7168, seed=22)]
+    for x in cases:
+        eps = float(np.float32(x.eps))
+        want, scale = _formula(x.routed, x.shared, x.g, x.W, eps)
+        got64 = oracle.forward(x.routed, x.shared, x.g, x.W, eps, precision="f64", lib=lib)
+        assert np.all(np.abs(got64 - want) <= 1e-12 * (scale + 1)), \
+            "double oracle differs from F.linear(F.rms_norm(...)) + shared"
+        got32 = oracle.forward(x.routed, x.shared, x.g, x.W, eps, lib=lib)
+        # FP32 rounding of sums of ~L terms stays far below 1e-5 of their scale
+        assert np.all(np.abs(got32 - want) <= 1e-5 * (scale + 1)), \
+            "FP32 oracle differs from F.linear(F.rms_norm(...)) + shared"
+        # a column range is the matching slice of the formula
+        got = oracle.forward(x.routed, x.shared, x.g, x.W, eps, 64, 128, precision="f64",
+                             lib=lib)
+        assert np.all(np.abs(got - want[:, 64:128]) <= 1e-12 * (scale[:, 64:128] + 1)), \
+            "column range differs from the formula's columns"
+
+
 ALL_PINS = (g_zero, constant_row, selection_matrix, shared_linearity, p_split,
-            column_concat, brute_force, no_norm)
+            column_concat, brute_force, no_norm, torch_formula)
