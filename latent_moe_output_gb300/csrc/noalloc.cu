@@ -32,16 +32,27 @@ void* g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_scratch_mutex;
 
 // Device address of the static scratch on the current device. The lookup runs
-// on the first call per device, with that device current.
+// on the first call per device, with that device current. A device this
+// library has no code for (anything but compute capability 10.3) is reported
+// as unsupported before the lookup, which would fail there; a failed lookup
+// clears the error it leaves in the runtime so later, unrelated error checks
+// do not see it.
 lt_status scratch_on_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return LT_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return LT_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_latent) != cudaSuccess || p == nullptr)
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return LT_ERR_CUDA;
+    if (major != 10 || minor != 3) return LT_ERR_UNSUPPORTED;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_latent) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return LT_ERR_CUDA;
+    }
     g_scratch_ptr[dev] = p;
   }
   *out = g_scratch_ptr[dev];

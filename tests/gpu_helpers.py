@@ -40,6 +40,38 @@ def oracle_rows(x: inputs.Inputs, rows, c0=0, c1=None) -> np.ndarray:
     return oracle.forward(r, s, x.g.cpu(), x.W.cpu(), x.eps, c0, c1)
 
 
+def oracle_all_rows(x: inputs.Inputs, c0=0, c1=None, chunk=64, workers=None) -> np.ndarray:
+    """FP32 oracle on every token row, [T, c1 - c0].
+
+    Rows of the tail never interact, so the token range is cut into chunks and
+    each chunk is one ordinary single-threaded oracle call; the chunks run
+    concurrently on the host's cores (ctypes releases the GIL during the call).
+    The result is exactly that of one call over all rows."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    lib = oracle.load()
+
+    def bits(t):
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    r, s, w = bits(x.routed), bits(x.shared), bits(x.W)
+    g = None if x.g is None else x.g.detach().cpu().float().numpy()
+    T, H = r.shape[1], w.shape[0]
+    c1 = H if c1 is None else c1
+    out = np.empty((T, c1 - c0), dtype=np.float32)
+
+    def one(t0):
+        t1 = min(T, t0 + chunk)
+        out[t0:t1] = oracle.forward(np.ascontiguousarray(r[:, t0:t1]),
+                                    np.ascontiguousarray(s[:, t0:t1]), g, w, x.eps, c0, c1,
+                                    lib=lib)
+
+    with ThreadPoolExecutor(max_workers=workers or os.cpu_count() or 4) as ex:
+        list(ex.map(one, range(0, T, chunk)))
+    return out
+
+
 def assert_parity(got: torch.Tensor, want: np.ndarray, what: str = ""):
     g = got.float().cpu()
     w = torch.from_numpy(np.asarray(want, dtype=np.float32))

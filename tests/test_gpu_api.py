@@ -41,26 +41,35 @@ def test_overlapping_output_is_rejected():
     assert e.value.status == Status.INVALID_ARG
 
 
-@pytest.mark.parametrize("T,c0,c1", [(16, 0, 1024), (16, 256, 512), (300, 0, 1024),
-                                     (300, 128, 896), (200, 0, 1024), (200, 128, 896)])
-def test_in_place_into_a_shared_partial(T, c0, c1):
-    """out aliasing shared[p] (the pages' in-place addmm_ into the shared
-    output): same values as the out-of-place call; columns outside the range
-    keep the partial's own values."""
-    x = gh.to_dev(inputs.make(3, T, 512, 1024, seed=T + c0))
-    ref = torch.full((T, 1024), float("nan"), dtype=torch.bfloat16, device="cuda")
-    gh.run(x, c0, c1, out=ref)
-    for p in (0, 2):
-        shared = x.shared.clone()
+@pytest.mark.parametrize("P,T,L,H,c0,c1", [
+    (3, 16, 512, 1024, 0, 1024), (3, 16, 512, 1024, 256, 512),     # decode kernel
+    (3, 300, 512, 1024, 0, 1024), (3, 300, 512, 1024, 128, 896),   # prefill, 256-col tiles
+    (3, 200, 512, 1024, 0, 1024), (3, 200, 512, 1024, 128, 896),   # prefill, 128-col tiles
+    (8, 1000, 2048, 7168, 0, 7168),                                # production widths
+])
+def test_in_place_into_a_shared_partial(P, T, L, H, c0, c1):
+    """out aliasing shared[p] (the pages' in-place addmm_ into the shared output)
+    matches the FP32 oracle on the original partials, leaves the columns outside
+    the range at the partial's own values, and equals the out-of-place call bit
+    for bit. T is not a multiple of 128 on the prefill path, so the shared-partial
+    boxes of one plane run into the next plane (and past the last one)."""
+    x = inputs.make(P, T, L, H, seed=T + c0)
+    xd = gh.to_dev(x)
+    want = gh.oracle_all_rows(x, c0, c1)
+    ref = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gh.run(xd, c0, c1, out=ref)
+    for p in (0, P - 1):
+        shared = xd.shared.clone()
         before = shared[p].clone()
-        ws = torch.empty(binding.latent_tail_workspace_size(3, T, 512, 1024),
+        ws = torch.empty(binding.latent_tail_workspace_size(P, T, L, H),
                          dtype=torch.uint8, device="cuda")
-        binding.latent_tail_forward_cols(x.routed, shared, x.g, x.W, shared[p], x.eps, c0, c1,
+        binding.latent_tail_forward_cols(xd.routed, shared, xd.g, xd.W, shared[p], x.eps, c0, c1,
                                          ws)
         binding.latent_tail_check()
-        assert torch.equal(shared[p][:, c0:c1].view(torch.int16), ref[:, c0:c1].view(torch.int16))
+        gh.assert_parity(shared[p][:, c0:c1], want, f"in place into shared[{p}]")
         assert torch.equal(shared[p][:, :c0], before[:, :c0])
         assert torch.equal(shared[p][:, c1:], before[:, c1:])
+        assert torch.equal(shared[p][:, c0:c1].view(torch.int16), ref[:, c0:c1].view(torch.int16))
 
 
 @pytest.mark.parametrize("T", [16, 512])

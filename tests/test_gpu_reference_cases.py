@@ -10,7 +10,9 @@ FP32 oracle.
 Same test, `_check_writes_only_its_own_shard`: each rank adds latent . W[start:end]^T
 into its own shared output in place, over its column shard [rank*H/tp,
 (rank+1)*H/tp) only; every other column stays bit-identical. Here that is
-latent_tail_project_cols with P = 1, out aliasing the single shared partial."""
+latent_tail_project_cols with P = 1, out aliasing the single shared partial, and
+the expectation is the FP32 oracle given the all-reduced routed partials and that
+rank's shared output as its only shared partial."""
 
 import numpy as np
 import pytest
@@ -74,6 +76,7 @@ def test_writes_only_its_own_shard(tp, weights):
             bits, bbits = local.view(torch.int16), before.view(torch.int16)
             assert torch.equal(bits[:, :start], bbits[:, :start]), f"rank {rank}: wrote below start"
             assert torch.equal(bits[:, end:], bbits[:, end:]), f"rank {rank}: wrote past end"
-            want = (before[:, start:end].double()
-                    + latent.double() @ Wd[start:end].double().t()).cpu().numpy()
+            # the FP32 oracle with this rank's shared output as the only partial:
+            # before[:, start:end] + F.linear(latent, W[start:end])
+            want = oracle.forward(routed, shared[rank][None], g, W, inputs.EPS, start, end)
             assert_parity(local[:, start:end], want, f"tp{tp} it{it} T{T} rank{rank}")

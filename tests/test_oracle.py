@@ -46,3 +46,15 @@ def test_fp32_oracle_within_fp32_rounding_of_double_at_production_width(oracle_l
     # the normalized latent has unit RMS up to the weight g and eps
     rms = np.sqrt(np.mean((y64 / x.g.double().numpy()) ** 2, axis=1))
     assert np.allclose(rms, 1.0, atol=1e-5)
+
+
+def test_chunked_concurrent_oracle_equals_one_call(oracle_lib):
+    """The GPU parity tests run the oracle over token ranges concurrently (rows
+    are independent); the stitched result is bit for bit the one-call result."""
+    import gpu_helpers as gh
+    from latent_moe_output_gb300 import inputs
+
+    x = inputs.make(3, 37, 64, 96, seed=8)
+    one = oracle.forward(x.routed, x.shared, x.g, x.W, x.eps, 8, 88, lib=oracle_lib)
+    many = gh.oracle_all_rows(x, 8, 88, chunk=5, workers=4)
+    assert np.array_equal(one, many)
