@@ -5,12 +5,21 @@
 
 A step is one call of the whole tail (routed reduce + RMSNorm, up-projection,
 shared-partial epilogue) on one batch of synthetic inputs. The default workload
-is the decode configuration (P=8, T=16, L=2048, H=7168). Inputs rotate over
-enough seeded sets that their total exceeds twice the L2 size, so every step
-streams W and the partials from HBM. Steps are replayed from CUDA graphs and
-timed with CUDA events on the launching stream, between a barrier and a device
-synchronize on both sides; with N > 1 each rank runs its own replica (token
-batches are independent, no collective) and the max time over ranks is used.
+is the largest benchmark configuration, the stress workload (P=16, T=16384,
+L=2048, H=7168, 1% of rows x100 and 1% x1e-3). Inputs rotate over enough seeded
+sets that their total exceeds twice the L2 size, so every step streams W and the
+partials from HBM. Steps are replayed from CUDA graphs and timed with CUDA
+events on the launching stream, between a barrier and a device synchronize on
+both sides; a timed region holds exactly K steps and is repeated (about one
+second of timed work in all, so the clock samples come from inside the regions),
+and the median region is reported. With N > 1 each rank runs its own replica
+(token batches are independent, no collective) and the max time over ranks is
+used.
+
+The line also carries, under "workloads", µs/call, tokens/s, the roofline of
+the dominant kernel and the single-call latency of every other benchmark
+configuration (decode P8 T16, the decode sweep T = 1..128, prefill P8 T8192 and
+the pre-reduced P=1 prefill).
 
 `single_call_us_median` is the median device time of one call with nothing else
 on the GPU before or after it (an eager call enqueued behind a spin kernel): the
@@ -47,13 +56,17 @@ L2_BYTES = 126 * 1024 * 1024  # replaced by the device's value at run time
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--workload", default="stress")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other benchmark configurations (the 'workloads' record)")
+    ap.add_argument("--repeats", type=int, default=0,
+                    help="timed regions of K steps (0: enough for about one second)")
     ap.add_argument("--T", type=int, default=0, help="override the workload's token count")
-    ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps (capped)")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps")
     ap.add_argument("--shards", type=int, default=0,
                     help="also time each step as N column-range calls covering [0, H)")
     return ap.parse_args()
@@ -319,6 +332,190 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+# The other benchmark configurations, measured after the headline workload and
+# reported under "workloads" in the same line.
+SUB_WORKLOADS = ("decode", "decode_T1", "decode_T8", "decode_T32", "decode_T64",
+                 "decode_T128", "prefill", "prefill_p1")
+
+
+def roofline_of(w, us_proj, us_call, hbm, tc_burst, peak_kind):
+    """Roofline of the dominant (projection) kernel and of the whole call. The
+    binding roofline is HBM unless the kernel's flops take longer at the tensor
+    peak than its bytes at the HBM peak (the P = 1 prefill)."""
+    P, T, L, H = w.P, w.T, w.L, w.H
+    pb, cb, fl = project_bytes(P, T, L, H), call_bytes(P, T, L, H), flops(T, L, H)
+    kname = "decode_kernel" if T <= 128 else "prefill_kernel"
+    proj_gbs = pb / (us_proj * 1e-6) / 1e9
+    if fl / (tc_burst * 1e12) > pb / (hbm * 1e9):
+        proj_tf = fl / (us_proj * 1e-6) / 1e12
+        roof = {"kernel": kname, "bound": "tensor", "achieved": round(proj_tf, 1),
+                "peak": tc_burst, "unit": "TFLOP/s", "frac": round(proj_tf / tc_burst, 4),
+                "traffic": None, "algorithmic_flops_per_launch": fl,
+                "us_per_launch": round(us_proj, 3), "peak_source": peak_kind}
+    else:
+        roof = {"kernel": kname, "bound": "hbm", "achieved": round(proj_gbs, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(proj_gbs / hbm, 4),
+                "traffic": profiled_traffic(kname, w.name, T),
+                "algorithmic_bytes_per_launch": pb, "us_per_launch": round(us_proj, 3),
+                "peak_source": peak_kind}
+    call_gbs = cb / (us_call * 1e-6) / 1e9
+    call_roof = {"achieved": round(call_gbs, 1), "peak": hbm, "unit": "GB/s",
+                 "frac": round(call_gbs / hbm, 4), "algorithmic_bytes_per_call": cb,
+                 "tensor_tflops": round(fl / (us_call * 1e-6) / 1e12, 2),
+                 "tensor_frac_of_burst_peak": round(fl / (us_call * 1e-6) / 1e12 / tc_burst, 4)}
+    return roof, call_roof
+
+
+class Bench:
+    """Timing of one workload: rotating input sets resident in HBM, steps replayed
+    from CUDA graphs, CUDA events on the launching stream."""
+
+    def __init__(self, w, args, dev, rank, world):
+        import torch
+
+        from latent_moe_output_gb300 import binding, inputs
+
+        self.torch, self.binding, self.inputs = torch, binding, inputs
+        self.w, self.args, self.dev, self.rank, self.world = w, args, dev, rank, world
+        P, T, L, H = w.P, w.T, w.L, w.H
+        props = torch.cuda.get_device_properties(dev)
+        self.l2 = getattr(props, "L2_cache_size", L2_BYTES) or L2_BYTES
+        binding.load_library()
+        self.ws_bytes = binding.latent_tail_workspace_size(P, T, L, H)
+        self.set_bytes = call_bytes(P, T, L, H) + self.ws_bytes
+        # enough sets that their total exceeds twice L2: every step reads from HBM
+        self.n_sets = max(2, -(-2 * self.l2 // self.set_bytes) + 1)
+        self.sets = []
+        for r in range(self.n_sets):
+            x = inputs.make(P, T, L, H, w.seed + 7919 * r + 104729 * rank, device=dev,
+                            outliers=w.outlier_rows)
+            out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+            self.sets.append((x, out, ws))
+        self.stream = torch.cuda.Stream(device=dev)
+
+    def step(self, i):
+        x, out, ws = self.sets[i % self.n_sets]
+        self.binding.latent_tail_forward(x.routed, x.shared, x.g, x.W, out, x.eps, ws,
+                                         self.stream)
+
+    def project_only(self, i):
+        T, L, H = self.w.T, self.w.L, self.w.H
+        x, out, ws = self.sets[i % self.n_sets]
+        y = ws[:T * L * 2].view(self.torch.bfloat16).view(T, L)
+        self.binding.latent_tail_project_cols(y, x.shared, x.W, out, 0, H, self.stream)
+
+    def warm(self, n):
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            for i in range(max(3, n)):
+                self.step(i)
+        self.binding.latent_tail_check(self.stream)
+        # rough per-call time, to size the timed regions of the extra workloads
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for i in range(5):
+                self.step(i)
+            e1.record(self.stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / 5
+
+    def timed(self, fn, steps, repeats):
+        """Seconds of each of `repeats` timed regions of exactly `steps` steps,
+        each region bracketed by a barrier and a device synchronize."""
+        torch = self.torch
+        chunk = min(steps, 50 * self.n_sets)
+        graphs, plan, left = {}, [], steps
+        while left > 0:
+            n = min(chunk, left)
+            if n not in graphs:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(self.stream):
+                    with torch.cuda.graph(g, stream=self.stream):
+                        for i in range(n):
+                            fn(i)
+                graphs[n] = g
+            plan.append(graphs[n])
+            left -= n
+        self.graph_calls = chunk
+        out = []
+        # CUDAGraph.replay() launches on the current stream: make it the stream the
+        # events are recorded on.
+        with torch.cuda.stream(self.stream):
+            for g in graphs.values():  # untimed replay: settle clocks and caches
+                g.replay()
+            self.stream.synchronize()
+            for _ in range(repeats):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                barrier(self.world)
+                torch.cuda.synchronize(self.dev)
+                e0.record(self.stream)
+                for g in plan:
+                    g.replay()
+                e1.record(self.stream)
+                torch.cuda.synchronize(self.dev)
+                barrier(self.world)
+                out.append(e0.elapsed_time(e1) / 1e3)
+        return out
+
+    def single_call_us(self, n):
+        """Median device time of one call with nothing else on the GPU before or
+        after it: a spin kernel keeps the GPU busy while the events and the call's
+        launches are enqueued, so the interval holds only the call's own time."""
+        torch = self.torch
+        single = []
+        with torch.cuda.stream(self.stream):
+            for i in range(self.n_sets + n):
+                torch.cuda._sleep(200000)  # ~100 us at 2 GHz
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(self.stream)
+                self.step(i)
+                b.record(self.stream)
+                b.synchronize()
+                if i >= self.n_sets:  # first round over the sets: warm-up
+                    single.append(a.elapsed_time(b) * 1e3)
+        self.binding.latent_tail_check(self.stream)
+        return max_over_ranks(statistics.median(single) * 1e-6, self.world) * 1e6
+
+    def release(self):
+        self.sets = []
+        self.torch.cuda.synchronize(self.dev)
+        self.torch.cuda.empty_cache()
+
+
+def region_plan(us_est, min_steps, target_s, max_repeats=200):
+    """Steps per timed region and number of regions: at least `min_steps` steps
+    and about 2 ms per region, repeated until about `target_s` seconds are timed."""
+    steps = max(min_steps, int(2000.0 / max(us_est, 1e-3)) + 1)
+    region_s = steps * us_est * 1e-6
+    repeats = int(min(max_repeats, max(3, round(target_s / max(region_s, 1e-9)))))
+    return steps, repeats
+
+
+def measure_extra(w, args, dev, rank, world, peak):
+    """µs/call, tokens/s, the roofline of the dominant kernel and the single-call
+    latency of one more benchmark configuration."""
+    b = Bench(w, args, dev, rank, world)
+    us_est = b.warm(args.warmup)
+    steps, repeats = region_plan(us_est, args.steps, 0.05)
+    t_call = max_over_ranks(statistics.median(b.timed(b.step, steps, repeats)), world)
+    t_proj = max_over_ranks(statistics.median(b.timed(b.project_only, steps, repeats)), world)
+    b.binding.latent_tail_check(b.stream)
+    us_call, us_proj = t_call / steps * 1e6, t_proj / steps * 1e6
+    roof, call_roof = roofline_of(w, us_proj, us_call, *peak)
+    rec = {"workload": w.name, "P": w.P, "T": w.T, "L": w.L, "H": w.H,
+           "us_per_call": round(us_call, 3),
+           "tokens_per_s": round(job_throughput(w.T, steps, world, t_call), 1),
+           "single_call_us_median": round(b.single_call_us(100 if w.T <= 128 else 5), 3),
+           "roofline": roof, "call_roofline": call_roof,
+           "timing": f"median of {repeats} regions of {steps} graph-replayed calls"}
+    b.release()
+    return rec
+
+
 def ours(args):
     import torch
 
@@ -332,87 +529,28 @@ def ours(args):
         w = dataclasses.replace(w, name=f"{w.name}_T{args.T}", T=args.T)
     P, T, L, H = w.P, w.T, w.L, w.H
     dev = torch.device("cuda", local)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", L2_BYTES) or L2_BYTES
-    lib = binding.load_library()
+    hbm, tc_burst, tc_sus, peak_kind = peaks()
+    peak = (hbm, tc_burst, peak_kind)
 
-    set_bytes = call_bytes(P, T, L, H) + binding.latent_tail_workspace_size(P, T, L, H)
-    n_sets = max(2, -(-2 * l2 // set_bytes) + 1)
-    sets = []
-    for r in range(n_sets):
-        x = inputs.make(P, T, L, H, w.seed + 7919 * r + 104729 * rank, device=dev,
-                        outliers=w.outlier_rows)
-        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-        ws = torch.empty(binding.latent_tail_workspace_size(P, T, L, H), dtype=torch.uint8,
-                         device=dev)
-        sets.append((x, out, ws))
-    stream = torch.cuda.Stream(device=dev)
-
-    def step(i):
-        x, out, ws = sets[i % n_sets]
-        binding.latent_tail_forward(x.routed, x.shared, x.g, x.W, out, x.eps, ws, stream)
-
-    def project_only(i):
-        x, out, ws = sets[i % n_sets]
-        y = ws[:T * L * 2].view(torch.bfloat16).view(T, L)
-        binding.latent_tail_project_cols(y, x.shared, x.W, out, 0, H, stream)
-
-    with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
-            step(i)
-    binding.latent_tail_check(stream)
-
-    chunk = min(args.steps, 50 * n_sets)
-
-    def capture(fn, n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(n):
-                    fn(i)
-        return g
-
-    def timed(fn, steps):
-        graphs = {}
-        plan = []
-        left = steps
-        while left > 0:
-            n = min(chunk, left)
-            if n not in graphs:
-                graphs[n] = capture(fn, n)
-            plan.append(graphs[n])
-            left -= n
-        # CUDAGraph.replay() launches on the current stream: make it `stream`,
-        # the stream the events are recorded on.
-        with torch.cuda.stream(stream):
-            for g in graphs.values():  # untimed replay: settle clocks and caches
-                g.replay()
-            stream.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            barrier(world)
-            torch.cuda.synchronize(dev)
-            e0.record(stream)
-            for g in plan:
-                g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            barrier(world)
-        return e0.elapsed_time(e1) / 1e3  # seconds
-
-    for _, out, _ in sets:  # poison outputs: the timed steps must overwrite them
+    b = Bench(w, args, dev, rank, world)
+    us_est = b.warm(args.warmup)
+    K = args.steps
+    # Exactly K steps per timed region; the region is repeated so that the timed
+    # time adds up to about a second (clock samples come from inside it).
+    repeats = args.repeats or int(min(2000, max(3, round(1.0 / max(K * us_est * 1e-6, 1e-9)))))
+    for _, out, _ in b.sets:  # poison outputs: the timed steps must overwrite them
         out.fill_(float("nan"))
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
-        t_step = timed(step, args.steps)
-    binding.latent_tail_check(stream)
-    written = min(args.steps, n_sets)
-    for _, out, _ in sets[:written]:
+        regions = b.timed(b.step, K, repeats)
+    binding.latent_tail_check(b.stream)
+    for _, out, _ in b.sets[:min(K, b.n_sets)]:
         if not torch.isfinite(out.float()).all():
             raise RuntimeError("timed steps did not write their outputs")
-    t_step = max_over_ranks(t_step, world)
-    t_proj = max_over_ranks(timed(project_only, args.steps), world)
-    binding.latent_tail_check(stream)
+    t_step = max_over_ranks(statistics.median(regions), world)
+    t_proj = max_over_ranks(statistics.median(b.timed(b.project_only, K, repeats)), world)
+    binding.latent_tail_check(b.stream)
+    graph_calls = b.graph_calls
 
     # Column-shard form: a step is N latent_tail_forward_cols calls whose ranges
     # (multiples of 8) tile [0, H); together they write the whole output.
@@ -421,25 +559,26 @@ def ours(args):
         bounds = [((H // 8) * k // args.shards) * 8 for k in range(args.shards)] + [H]
 
         def shard_step(i):
-            x, out, ws = sets[i % n_sets]
+            x, out, ws = b.sets[i % b.n_sets]
             for k in range(args.shards):
                 binding.latent_tail_forward_cols(x.routed, x.shared, x.g, x.W, out, x.eps,
-                                                 bounds[k], bounds[k + 1], ws, stream)
+                                                 bounds[k], bounds[k + 1], ws, b.stream)
 
         # The same shards with the latent computed once per step: one norm call,
         # then N projection calls over [0, H).
         def shard_step_norm_once(i):
-            x, out, ws = sets[i % n_sets]
+            x, out, ws = b.sets[i % b.n_sets]
             y = ws[:T * L * 2].view(torch.bfloat16).view(T, L)
-            binding.latent_tail_norm(x.routed, x.g, y, x.eps, stream)
+            binding.latent_tail_norm(x.routed, x.g, y, x.eps, b.stream)
             for k in range(args.shards):
                 binding.latent_tail_project_cols(y, x.shared, x.W, out, bounds[k], bounds[k + 1],
-                                                 stream)
+                                                 b.stream)
 
-        shard_steps = max(1, min(args.steps, 20))
-        t_shards = max_over_ranks(timed(shard_step, shard_steps), world)
-        t_once = max_over_ranks(timed(shard_step_norm_once, shard_steps), world)
-        binding.latent_tail_check(stream)
+        shard_steps = max(1, min(K, 20))
+        t_shards = max_over_ranks(statistics.median(b.timed(shard_step, shard_steps, 3)), world)
+        t_once = max_over_ranks(statistics.median(b.timed(shard_step_norm_once, shard_steps, 3)),
+                                world)
+        binding.latent_tail_check(b.stream)
         shard_line = {"calls_per_step": args.shards, "steps": shard_steps,
                       "us_per_step": round(t_shards / shard_steps * 1e6, 3),
                       "tokens_per_s": round(job_throughput(T, shard_steps, world, t_shards), 1),
@@ -447,101 +586,70 @@ def ours(args):
                       "norm_once_us_per_step": round(t_once / shard_steps * 1e6, 3),
                       "norm_once_note": "latent_tail_norm once, then N latent_tail_project_cols"}
 
-    # One call at a time, with nothing before or after it on the GPU (no overlap
-    # with a neighbouring call): a spin kernel keeps the GPU busy while the
-    # events and the call's two kernel launches are enqueued, so the interval
-    # holds only the call's own device time.
-    single = []
-    with torch.cuda.stream(stream):
-        for i in range(max(100, 2 * n_sets) if T <= 128 else 3 * n_sets):
-            torch.cuda._sleep(200000)  # ~100 us at 2 GHz
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            step(i)
-            b.record(stream)
-            b.synchronize()
-            if i >= n_sets:  # first round over the sets: warm-up
-                single.append(a.elapsed_time(b) * 1e3)
-    binding.latent_tail_check(stream)
-    us_single = max_over_ranks(statistics.median(single) * 1e-6, world) * 1e6
+    us_single = b.single_call_us(100 if T <= 128 else 5)
 
     # End to end through the host-buffer entry point: every step takes its
-    # partials from page-locked host memory and leaves its result there. Each
-    # input set has its own pinned host copy; steps rotate over them as the
-    # device-resident steps do, and are replayed from CUDA graphs the same way.
-    e2e_steps = args.e2e_steps or min(args.steps, 500)
-    hsets = [(x.routed.cpu().pin_memory(), x.shared.cpu().pin_memory()) for x, _, _ in sets]
+    # partials from page-locked host memory and leaves its result there. The
+    # host sets rotate like the device-resident ones (one set when a set exceeds
+    # 1 GB: the host link, not L2, bounds such a step).
+    e2e_steps = args.e2e_steps or K
+    n_host = b.n_sets if b.set_bytes < (1 << 30) else 1
+    hsets = [(x.routed.cpu().pin_memory(), x.shared.cpu().pin_memory())
+             for x, _, _ in b.sets[:n_host]]
     h_out = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
     h_ws = torch.empty(binding.latent_tail_host_workspace_size(P, T, L, H), dtype=torch.uint8,
                        device=dev)
 
     def e2e_step(i):
-        x = sets[i % n_sets][0]
-        hr, hs = hsets[i % n_sets]
-        binding.latent_tail_forward_host(hr, hs, x.g, x.W, h_out, x.eps, h_ws, stream)
+        x = b.sets[i % b.n_sets][0]
+        hr, hs = hsets[i % n_host]
+        binding.latent_tail_forward_host(hr, hs, x.g, x.W, h_out, x.eps, h_ws, b.stream)
 
     # The same step with explicit staging copies issued from Python around the
     # device entry point (pinned host -> device, call, device -> pinned host).
-    d_in = {"routed": torch.empty_like(sets[0][0].routed),
-            "shared": torch.empty_like(sets[0][0].shared),
+    d_in = {"routed": torch.empty_like(b.sets[0][0].routed),
+            "shared": torch.empty_like(b.sets[0][0].shared),
             "out": torch.empty(T, H, dtype=torch.bfloat16, device=dev)}
 
     def staged_step(i):
-        x, _, ws = sets[i % n_sets]
-        hr, hs = hsets[i % n_sets]
+        x, _, ws = b.sets[i % b.n_sets]
+        hr, hs = hsets[i % n_host]
         d_in["routed"].copy_(hr, non_blocking=True)
         d_in["shared"].copy_(hs, non_blocking=True)
         binding.latent_tail_forward(d_in["routed"], d_in["shared"], x.g, x.W, d_in["out"],
-                                    x.eps, ws, stream)
+                                    x.eps, ws, b.stream)
         h_out.copy_(d_in["out"], non_blocking=True)
 
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(b.stream):
         for i in range(3):
             e2e_step(i)
-    stream.synchronize()
-    t_e2e = max_over_ranks(timed(e2e_step, e2e_steps), world)
-    binding.latent_tail_check(stream)
+    b.stream.synchronize()
+    e2e_reps = 3
+    t_e2e = max_over_ranks(statistics.median(b.timed(e2e_step, e2e_steps, e2e_reps)), world)
+    binding.latent_tail_check(b.stream)
     if not torch.isfinite(h_out.float()).all():
         raise RuntimeError("end-to-end steps did not produce a finite result")
-    t_staged = max_over_ranks(timed(staged_step, e2e_steps), world)
-    binding.latent_tail_check(stream)
+    t_staged = max_over_ranks(statistics.median(b.timed(staged_step, e2e_steps, e2e_reps)), world)
+    binding.latent_tail_check(b.stream)
+    n_sets, set_bytes, l2 = b.n_sets, b.set_bytes, b.l2
+    del hsets, h_out, h_ws, d_in
+    b.release()
+
+    extra = []
+    if not args.no_workloads:
+        for name in SUB_WORKLOADS:
+            if name != w.name:
+                extra.append(measure_extra(workload(name), args, dev, rank, world, peak))
 
     if rank != 0:
         return
-    hbm, tc_burst, tc_sus, peak_kind = peaks()
-    tokens_per_s = job_throughput(T, args.steps, world, t_step)
-    us_call = t_step / args.steps * 1e6
-    us_proj = t_proj / args.steps * 1e6
-    pb = project_bytes(P, T, L, H)
-    cb = call_bytes(P, T, L, H)
-    fl = flops(T, L, H)
-    proj_gbs = pb / (us_proj * 1e-6) / 1e9
-    call_gbs = cb / (us_call * 1e-6) / 1e9
-    # The binding roofline of the projection kernel: HBM unless its flops take
-    # longer at the tensor peak than its bytes at the HBM peak (P = 1 prefill).
-    tensor_bound = fl / (tc_burst * 1e12) > pb / (hbm * 1e9)
-    kname = "decode_kernel" if T <= 128 else "prefill_kernel"
-    if tensor_bound:
-        proj_tf = fl / (us_proj * 1e-6) / 1e12
-        roof = {"kernel": kname, "bound": "tensor", "achieved": round(proj_tf, 1),
-                "peak": tc_burst, "unit": "TFLOP/s", "frac": round(proj_tf / tc_burst, 4),
-                "traffic": None, "algorithmic_flops_per_launch": fl,
-                "us_per_launch": round(us_proj, 3), "peak_source": peak_kind}
-    else:
-        roof = {"kernel": kname, "bound": "hbm", "achieved": round(proj_gbs, 1), "peak": hbm,
-                "unit": "GB/s", "frac": round(proj_gbs / hbm, 4),
-                "traffic": profiled_traffic(kname, w.name, T),
-                "algorithmic_bytes_per_launch": pb, "us_per_launch": round(us_proj, 3),
-                "peak_source": peak_kind}
-    call_roof = {"achieved": round(call_gbs, 1), "peak": hbm, "unit": "GB/s",
-                 "frac": round(call_gbs / hbm, 4), "algorithmic_bytes_per_call": cb,
-                 "tensor_tflops": round(fl / (us_call * 1e-6) / 1e12, 2),
-                 "tensor_frac_of_burst_peak": round(fl / (us_call * 1e-6) / 1e12 / tc_burst, 4)}
+    us_call = t_step / K * 1e6
+    us_proj = t_proj / K * 1e6
+    roof, call_roof = roofline_of(w, us_proj, us_call, *peak)
     line = {
-        "metric": "latent-tail tokens/s", "value": round(tokens_per_s, 1), "unit": "tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(t_step / args.steps * 1e3, 6), "us_per_call": round(us_call, 3),
+        "metric": "latent-tail tokens/s", "value": round(job_throughput(T, K, world, t_step), 1),
+        "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(t_step / K * 1e3, 6), "us_per_call": round(us_call, 3),
         "single_call_us_median": round(us_single, 3),
         **({"column_shards": shard_line} if shard_line else {}),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -550,10 +658,11 @@ def ours(args):
                    "parallelism": f"replicas{world}",
                    "l2": f"inputs rotate over {n_sets} sets, {n_sets * set_bytes / 2**20:.0f} MiB"
                          f" > 2x L2 ({l2 / 2**20:.0f} MiB)",
-                   "timing": "CUDA graphs of up to %d calls, CUDA events on the launching stream"
-                             % chunk},
+                   "timing": f"median of {repeats} timed regions of exactly {K} steps, each "
+                             f"replayed from CUDA graphs of up to {graph_calls} calls and timed "
+                             "with CUDA events on the launching stream"},
         "roofline": roof, "call_roofline": call_roof,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 2 * K,
         "clocks": clocks.summary(),
         "e2e": {"value": round(job_throughput(T, e2e_steps, world, t_e2e), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": P * T * L * 2 + P * T * H * 2,
@@ -563,10 +672,12 @@ def ours(args):
                        + ("kernels read/write them across the host link"
                           if T <= 128 else "staged with one copy per tensor") + ")",
                 "staged_copies_us_per_step": round(t_staged / e2e_steps * 1e6, 3),
-                "timing": "CUDA graphs, CUDA events, inputs rotate over pinned host sets"},
+                "timing": f"median of {e2e_reps} regions, CUDA graphs, CUDA events, "
+                          f"{n_host} pinned host set(s)"},
+        "workloads": extra,
     }
-    if not args.no_cpu_baseline and world >= 1:
-        line["cpu_baseline"] = cpu_baseline(w)
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, max_tokens=1024)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -49,8 +49,7 @@ def build(out: Path = OUT, extra_flags=(), verbose: bool = False, force: bool = 
             return out
     home = cuda_home()
     nvcc = str(home / "bin" / "nvcc")
-    tag = "tuning" if extra_flags else "release"
-    objdir = BUILD / tag
+    objdir = BUILD / ("release" if not extra_flags else "variant")
     objdir.mkdir(parents=True, exist_ok=True)
     flags = nvcc_flags(extra_flags)
 
@@ -80,7 +79,4 @@ def build(out: Path = OUT, extra_flags=(), verbose: bool = False, force: bool = 
 
 
 if __name__ == "__main__":
-    args = sys.argv[1:]
-    extra = ["-DLT_TUNING"] if "--tuning" in args else []
-    target = OUT if not extra else PKG / "_lib" / "liblatent_tail_tuning.so"
-    print(build(target, extra_flags=extra, verbose="-v" in args, force=True))
+    print(build(verbose="-v" in sys.argv[1:], force=True))

@@ -8,7 +8,6 @@
 
 #include <algorithm>
 #include <cmath>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -161,22 +160,6 @@ size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
 lt_status launch_status(cudaError_t e) { return e == cudaSuccess ? LT_OK : LT_ERR_CUDA; }
 
-bool norm_prefetches_w() {
-#ifdef LT_TUNING
-  const char* v = std::getenv("LT_NORM_PREFETCH");
-  if (v) return std::atoi(v) != 0;
-#endif
-  return true;
-}
-
-bool norm_prefetches_routed() {
-#ifdef LT_TUNING
-  const char* v = std::getenv("LT_NORM_PF_ROUTED");
-  if (v) return std::atoi(v) != 0;
-#endif
-  return true;
-}
-
 lt_status run_project(const lt::ProjectArgs& a, const lt::DeviceInfo& dev, cudaStream_t s) {
   if (a.T <= lt::kDecodeMaxTokens) return launch_status(lt::launch_decode(a, dev, s));
   return launch_status(lt::launch_prefill(a, dev, s));
@@ -212,7 +195,7 @@ lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const flo
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint16_t* y = static_cast<uint16_t*>(ws);
   lt::NormArgs na{routed, g, y, P, T, L, eps, nullptr, 0, false};
-  if (T <= lt::kDecodeMaxTokens && norm_prefetches_w()) {
+  if (T <= lt::kDecodeMaxTokens) {
     // The decode kernel streams W in whole 128-row tiles covering [c0, c1).
     const int r0 = c0 / lt::kDecodeTileRows * lt::kDecodeTileRows;
     const int r1 = std::min(H, (c1 + lt::kDecodeTileRows - 1) / lt::kDecodeTileRows *
@@ -224,7 +207,7 @@ lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const flo
     }
     // (not for page-locked host partials: the bulk L2 prefetch is only used on
     // device memory)
-    na.prefetch_routed = routed_in_device_memory && norm_prefetches_routed();
+    na.prefetch_routed = routed_in_device_memory;
   }
   if ((st = launch_status(lt::launch_norm(na, true, *dev, s))) != LT_OK) return st;
   const lt::ProjectArgs pa{y, shared, W, out, P, T, L, H, c0, c1, true, early_trigger};

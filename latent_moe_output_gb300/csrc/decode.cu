@@ -299,14 +299,6 @@ int next_pow2_at_least(int v, int lo) {
   return r;
 }
 
-#ifdef LT_TUNING
-#include <cstdlib>
-int env_int(const char* name, int dflt) {
-  const char* s = std::getenv(name);
-  return s ? std::atoi(s) : dflt;
-}
-#endif
-
 }  // namespace
 
 cudaError_t setup_decode(const DeviceInfo&) {
@@ -356,11 +348,6 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
                     static_cast<long>(stage_bytes);
     stages = static_cast<int>(std::max<long>(1, std::min<long>({st, p.total_kb, kMaxStages})));
   }
-#ifdef LT_TUNING
-  ks = env_int("LT_DECODE_KS", ks);
-  stages = std::min(std::max(1, env_int("LT_DECODE_STAGES", stages)),
-                    std::min(kMaxStages, ceil_div(p.total_kb, ks)));
-#endif
   const size_t ring = static_cast<size_t>(stages) * stage_bytes;
   p.ks = ks;
   p.kb_per_cta = ceil_div(p.total_kb, ks);
@@ -372,9 +359,6 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
   p.tmem_cols = next_pow2_at_least(p.npad, 32);
   p.pdl = a.pdl ? 1 : 0;
   p.trigger_after_issue = a.early_trigger ? 1 : 0;
-#ifdef LT_TUNING
-  p.trigger_after_issue = env_int("LT_DECODE_TRIGGER", p.trigger_after_issue);
-#endif
   p.err = dev.err_word;
   const int tile_first = a.col_start / kBlockM;
   const int tile_last = (a.col_end - 1) / kBlockM;

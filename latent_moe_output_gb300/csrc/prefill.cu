@@ -465,14 +465,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-#ifdef LT_TUNING
-#include <cstdlib>
-int env_int(const char* name, int dflt) {
-  const char* s = std::getenv(name);
-  return s ? std::atoi(s) : dflt;
-}
-#endif
-
 }  // namespace
 
 cudaError_t setup_prefill(const DeviceInfo&) {
@@ -497,9 +489,6 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   // A fixed function of T (never of the column range), so that every output
   // element is computed the same way whatever range a call asks for.
   p.tile_h = a.T <= 2 * kTileT ? kNarrowTileH : kTileH;
-#ifdef LT_TUNING
-  p.tile_h = env_int("LT_PREFILL_TILE_H", p.tile_h) == kNarrowTileH ? kNarrowTileH : kTileH;
-#endif
   p.htile0 = a.col_start / p.tile_h;
   p.n_htiles = (a.col_end - 1) / p.tile_h - p.htile0 + 1;
   p.n_tpairs = ceil_div(a.T, 2 * kTileT);
@@ -512,20 +501,12 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   } else if (p.tile_h == kNarrowTileH) {  // 24 KB stages: two more fit beside the slots
     p.stages = kMaxStages;
   }
-#ifdef LT_TUNING
-  p.stages = std::min(std::max(1, env_int("LT_PREFILL_STAGES", p.stages)), kMaxStages);
-  p.slots = std::min(std::max(1, env_int("LT_PREFILL_SLOTS", p.slots)), kMaxSlots);
-#endif
   const size_t smem = smem_bytes(p.stages, p.slots, p.tile_h);
   if (smem > kSmemLimit) return cudaErrorInvalidConfiguration;
   p.pdl = a.pdl ? 1 : 0;
   p.err = dev.err_word;
   const long long tiles = static_cast<long long>(p.n_htiles) * p.n_tpairs;
   p.stage_sums = tiles <= dev.num_sms / 2 ? 1 : 0;  // one tile per pair at most
-#ifdef LT_TUNING
-  p.stage_sums = env_int("LT_PREFILL_STAGE_SUMS", p.stage_sums);
-  if (tiles > dev.num_sms / 2) p.stage_sums = 0;
-#endif
   const int grid = 2 * static_cast<int>(std::min<long long>(dev.num_sms / 2, tiles));
 
   // The shared partials as one 2-D tensor [P*T rows, H columns]: the box for
