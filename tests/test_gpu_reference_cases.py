@@ -78,5 +78,8 @@ def test_writes_only_its_own_shard(tp, weights):
             assert torch.equal(bits[:, end:], bbits[:, end:]), f"rank {rank}: wrote past end"
             # the FP32 oracle with this rank's shared output as the only partial:
             # before[:, start:end] + F.linear(latent, W[start:end])
-            want = oracle.forward(routed, shared[rank][None], g, W, inputs.EPS, start, end)
+            # (zero partials next to it keep the partial count equal to routed's)
+            only = torch.zeros_like(shared)
+            only[0] = shared[rank]
+            want = oracle.forward(routed, only, g, W, inputs.EPS, start, end)
             assert_parity(local[:, start:end], want, f"tp{tp} it{it} T{T} rank{rank}")
