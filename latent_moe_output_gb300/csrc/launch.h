@@ -16,9 +16,11 @@ constexpr uint32_t kErrWaitTimeout = 1u;
 constexpr int kDecodeMaxTokens = 128;
 
 // Encodes a 2-D bf16 row-major [rows, cols] tensor map with a (64 x box_rows)
-// box and 128-byte swizzle. Returns false if the driver rejects it.
+// box and 128-byte swizzle. `promote_l2` asks L2 to fetch 256-byte sectors
+// (useful when the neighbouring bytes are read soon after). Returns false if
+// the driver rejects it.
 bool make_map_bf16_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                         uint32_t box_rows);
+                         uint32_t box_rows, bool promote_l2 = true);
 
 struct DeviceInfo {
   int device;
