@@ -219,7 +219,7 @@ lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const flo
 namespace lt {
 
 bool make_map_bf16_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                         uint32_t box_rows, bool promote_l2) {
+                         uint32_t box_rows) {
   if (g_encode == nullptr) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
@@ -228,8 +228,7 @@ bool make_map_bf16_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint
   const CUresult r =
       g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                box, estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               promote_l2 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_NONE,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

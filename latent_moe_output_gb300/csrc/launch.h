@@ -16,11 +16,11 @@ constexpr uint32_t kErrWaitTimeout = 1u;
 constexpr int kDecodeMaxTokens = 128;
 
 // Encodes a 2-D bf16 row-major [rows, cols] tensor map with a (64 x box_rows)
-// box and 128-byte swizzle. `promote_l2` asks L2 to fetch 256-byte sectors
-// (useful when the neighbouring bytes are read soon after). Returns false if
-// the driver rejects it.
+// box and 128-byte swizzle, without L2 sector promotion: every box reads
+// 128-byte row pieces whose neighbours are read much later, if at all (see the
+// prefill kernel's shared-partial map). Returns false if the driver rejects it.
 bool make_map_bf16_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                         uint32_t box_rows, bool promote_l2 = true);
+                         uint32_t box_rows);
 
 struct DeviceInfo {
   int device;

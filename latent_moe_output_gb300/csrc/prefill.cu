@@ -65,15 +65,23 @@ constexpr uint32_t kTmemCols = 2 * kTileH;
 constexpr size_t kSmemLimit = 226 * 1024;  // + static shared memory <= opt-in maximum
 
 // Shared memory splits between the operand ring (feeds the MMAs from L2) and
-// the shared-partial ring (feeds the epilogue from HBM); both hide latency,
-// so each gets as many bytes in flight as the other allows.
-constexpr int kDefaultStages = 4;
-constexpr int kDefaultSlots = 5;
+// the shared-partial ring (feeds the epilogue from HBM); both hide latency, so
+// the split follows the share of the shared-partial bytes, i.e. P (measured,
+// projection us, same box): P = 8, T = 8192: 4 + 6 216.7, 4 + 5 221.5, 3 + 7
+// 239.2, 3 + 8 239.9; P = 16, T = 16384: 3 + 8 669, 3 + 7 676, 4 + 6 682,
+// 4 + 5 701.
+constexpr int kStagesFewPartials = 4;  // 2 <= P <= 8
+constexpr int kSlotsFewPartials = 6;
+constexpr int kStagesManyPartials = 3;  // P > 8
+constexpr int kSlotsManyPartials = 8;
 // With a single shared partial the epilogue needs far fewer bytes in flight and
 // the tensor cores bind, so the operand ring gets them: P = 1, T = 8192 ran at
 // 172.1 us with 6 + 2 against 175.5 us with 4 + 5.
 constexpr int kSinglePartialStages = 6;
 constexpr int kSinglePartialSlots = 2;
+// 128-column tiles (T <= 256): 24 KB stages, six of them beside five slots.
+constexpr int kNarrowStages = 6;
+constexpr int kNarrowSlots = 5;
 
 size_t smem_bytes(int stages, int slots, int tile_h) {
   return 1024 + static_cast<size_t>(stages) * stage_bytes_for(tile_h) +
@@ -493,14 +501,22 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   p.n_htiles = (a.col_end - 1) / p.tile_h - p.htile0 + 1;
   p.n_tpairs = ceil_div(a.T, 2 * kTileT);
   p.total_kb = ceil_div(a.L, kBlockK);
-  p.stages = kDefaultStages;
-  p.slots = kDefaultSlots;
   if (a.P == 1) {  // one box per chunk: the operand ring gets the bytes (measured)
     p.stages = kSinglePartialStages;
     p.slots = kSinglePartialSlots;
-  } else if (p.tile_h == kNarrowTileH) {  // 24 KB stages: two more fit beside the slots
-    p.stages = kMaxStages;
+  } else if (p.tile_h == kNarrowTileH) {
+    p.stages = kNarrowStages;
+    p.slots = kNarrowSlots;
+  } else if (a.P <= 8) {
+    p.stages = kStagesFewPartials;
+    p.slots = kSlotsFewPartials;
+  } else {
+    p.stages = kStagesManyPartials;
+    p.slots = kSlotsManyPartials;
   }
+  // the barrier arrays hold kMaxStages / kMaxSlots entries
+  if (p.stages < 1 || p.stages > kMaxStages || p.slots < 1 || p.slots > kMaxSlots)
+    return cudaErrorInvalidConfiguration;
   const size_t smem = smem_bytes(p.stages, p.slots, p.tile_h);
   if (smem > kSmemLimit) return cudaErrorInvalidConfiguration;
   p.pdl = a.pdl ? 1 : 0;
@@ -512,17 +528,16 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   // The shared partials as one 2-D tensor [P*T rows, H columns]: the box for
   // (partial p, tokens t0..t0+127) starts at row p*T + t0. Rows past T inside
   // a partial belong to the next partial and are never stored; rows past P*T
-  // and columns past H read as zero. No 256-byte L2 promotion here: the other
-  // 128 bytes of each sector belong to the next column chunk, read only after
-  // all P partials of this one, by which time the read-once stream has evicted
-  // them (streaming this map's boxes alone in this order measured 8% slower
-  // with promotion).
+  // and columns past H read as zero. No tensor map asks for 256-byte L2
+  // promotion: here the other 128 bytes of each sector belong to the next
+  // column chunk, read only after all P partials of this one, by which time the
+  // read-once stream has evicted them. Promotion on this map cost 22% of the
+  // stress projection (901 against 704 us) and 12% of the prefill one.
   CUtensorMap y_map, w_map, s_map;
   if (!make_map_bf16_sw128(&y_map, a.y, a.T, a.L, kTileT)) return cudaErrorInvalidValue;
   if (!make_map_bf16_sw128(&w_map, a.W, a.H, a.L, static_cast<uint32_t>(p.tile_h / 2)))
     return cudaErrorInvalidValue;
-  if (!make_map_bf16_sw128(&s_map, a.shared, static_cast<uint64_t>(a.P) * a.T, a.H, kTileT,
-                           /*promote_l2=*/false))
+  if (!make_map_bf16_sw128(&s_map, a.shared, static_cast<uint64_t>(a.P) * a.T, a.H, kTileT))
     return cudaErrorInvalidValue;
 
   cudaLaunchConfig_t cfg{};
