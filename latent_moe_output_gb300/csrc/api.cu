@@ -210,7 +210,7 @@ lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const flo
     na.prefetch_routed = routed_in_device_memory;
   }
   if ((st = launch_status(lt::launch_norm(na, true, *dev, s))) != LT_OK) return st;
-  const lt::ProjectArgs pa{y, shared, W, out, P, T, L, H, c0, c1, true, early_trigger};
+  const lt::ProjectArgs pa{y, shared, W, out, P, T, L, H, c0, c1, true, early_trigger, true};
   return run_project(pa, *dev, s);
 }
 
@@ -360,7 +360,12 @@ LT_API lt_status latent_tail_project_cols(const uint16_t* latent, const uint16_t
     return LT_ERR_INVALID_ARG;
   const lt::DeviceInfo* dev = nullptr;
   if ((st = current_device(&dev)) != LT_OK) return st;
-  const lt::ProjectArgs pa{latent, shared, W, out, P, T, L, H, col_start, col_end, false, false};
+  // The decode kernel is launched as a programmatic dependent with every read
+  // after its dependency wait: back-to-back calls overlap one launch's start-up
+  // (barrier set-up, TMEM allocation) with the previous launch's tail.
+  const bool dep = T <= lt::kDecodeMaxTokens;
+  const lt::ProjectArgs pa{latent, shared, W, out, P,   T,   L,    H,
+                           col_start, col_end, dep, dep, false};
   return run_project(pa, *dev, reinterpret_cast<cudaStream_t>(stream));
 }
 

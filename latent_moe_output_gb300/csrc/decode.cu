@@ -60,6 +60,7 @@ struct DecodeParams {
   uint32_t ssum_offset;  // byte offsets (from the 1024-aligned base) of the
   uint32_t slot_offset;  // shared-partial sums and of the received K-slice partials
   int pdl;
+  int inputs_ready;         // W and shared complete at launch (only y is awaited)
   int trigger_after_issue;  // allow dependents once the last W copy is issued
   uint32_t* err;
 };
@@ -123,14 +124,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&acc_bar), 1);
     abort_flag = 0;
     mbar_fence_init();
-    // W does not depend on the preceding kernel: request the first stages now,
-    // before the rest of the set-up, so the HBM stream starts at once.
-    for (int i = 0; i < pre; ++i) {
-      const uint32_t fb = smem_u32(&full_bar[i]);
-      mbar_arrive_expect_tx(fb, stage_bytes);
-      tma_load_2d(sbase + static_cast<uint32_t>(i) * stage_bytes, &w_map, fb,
-                  (kb_begin + i) * kBlockK, h0);
-    }
+    // When W does not depend on the preceding kernel, request the first stages
+    // now, before the rest of the set-up, so the HBM stream starts at once.
+    if (!p.pdl || p.inputs_ready)
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t fb = smem_u32(&full_bar[i]);
+        mbar_arrive_expect_tx(fb, stage_bytes);
+        tma_load_2d(sbase + static_cast<uint32_t>(i) * stage_bytes, &w_map, fb,
+                    (kb_begin + i) * kBlockK, h0);
+      }
   }
   if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), static_cast<uint32_t>(p.tmem_cols));
   tc_fence_before();
@@ -142,11 +144,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0 && nkb > 0) {
       // ---------------- TMA producer ----------------
-      if (p.pdl) pdl_wait();  // y is written by the preceding norm kernel
+      if (p.pdl) pdl_wait();  // y is written by the preceding kernel
       for (int i = 0; i < pre; ++i) {
         const uint32_t st = sbase + static_cast<uint32_t>(i) * stage_bytes;
-        tma_load_2d(st + kWStageBytes, &y_map, smem_u32(&full_bar[i]), (kb_begin + i) * kBlockK,
-                    0);
+        const uint32_t fb = smem_u32(&full_bar[i]);
+        if (p.pdl && !p.inputs_ready) {  // W after the wait too
+          mbar_arrive_expect_tx(fb, stage_bytes);
+          tma_load_2d(st, &w_map, fb, (kb_begin + i) * kBlockK, h0);
+        }
+        tma_load_2d(st + kWStageBytes, &y_map, fb, (kb_begin + i) * kBlockK, 0);
       }
       int issued = pre;
       for (int i = pre; i < nkb; ++i) {
@@ -190,10 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue warps 2..5 ----------------
     // (a) While W streams in: sum the P shared partials of this CTA's rows,
-    //     p ascending in FP32, into shared memory. Independent of the norm kernel:
-    //     the work that wrote the partials finished before this kernel launched
-    //     (the norm kernel waited for it before releasing this one), so they are
-    //     read from L2 without waiting, never through a possibly stale L1.
+    //     p ascending in FP32, into shared memory. After a norm kernel of the same
+    //     call they are read without waiting: the work that wrote them finished
+    //     before that kernel released this one. Read from L2, never through a
+    //     possibly stale L1.
+    if (p.pdl && !p.inputs_ready) pdl_wait();
     const int et = threadIdx.x - 64;
     const size_t plane = static_cast<size_t>(p.T) * p.H;
     const int items = p.T * groups;
@@ -358,6 +365,7 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
       ring + ((static_cast<size_t>(p.npad) * rpc * 4 + 1023) & ~size_t(1023)));
   p.tmem_cols = next_pow2_at_least(p.npad, 32);
   p.pdl = a.pdl ? 1 : 0;
+  p.inputs_ready = a.inputs_ready ? 1 : 0;
   p.trigger_after_issue = a.early_trigger ? 1 : 0;
   p.err = dev.err_word;
   const int tile_first = a.col_start / kBlockM;

@@ -59,11 +59,17 @@ struct ProjectArgs {
   uint16_t* out;           // [T,H]
   int P, T, L, H;
   int col_start, col_end;
-  bool pdl;                // launched right after the norm kernel, may overlap it
+  bool pdl;                // launched as a programmatic dependent: may start before the
+                           // preceding kernel on the stream has finished
   // Decode kernel: let the next kernel on the stream launch as soon as each CTA
   // has issued its last W copy (else once its MMAs are done). Earlier lets the
   // next call's norm kernel prefetch its W into L2 during this call's tail.
   bool early_trigger;
+  // Everything but y was complete when this kernel was released: the preceding
+  // kernel is the norm kernel of the same call, which waited for all earlier work
+  // before releasing it, so W and the shared partials may be read before the
+  // dependency wait. Otherwise (pdl without it) every input is read after the wait.
+  bool inputs_ready;
 };
 
 cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const DeviceInfo& dev,
