@@ -300,7 +300,8 @@ def reference_arm(args):
     oracle.forward(x1.routed, x1.shared, x1.g, x1.W, x1.eps, lib=lib)
     per_tok = time.perf_counter() - t0
     per_step_budget = 120.0 / total
-    n = int(max(1, min(w.T, per_step_budget / max(per_tok, 1e-9))))
+    # at most 2048 tokens per step, so that the sample's inputs stay small on the host
+    n = int(max(1, min(w.T, 2048, per_step_budget / max(per_tok, 1e-9))))
     # When even one token per step exceeds the budget (many steps), a step is one
     # token over the first `width` output columns and counts as width/H of a
     # token: the oracle's time per token is proportional to the columns it
