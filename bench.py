@@ -595,8 +595,12 @@ def ours(args):
     # 1 GB: the host link, not L2, bounds such a step).
     e2e_steps = args.e2e_steps or K
     n_host = b.n_sets if b.set_bytes < (1 << 30) else 1
-    hsets = [(x.routed.cpu().pin_memory(), x.shared.cpu().pin_memory())
-             for x, _, _ in b.sets[:n_host]]
+    def pinned_copy(t):  # page-locked host copy without a pageable intermediate
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
+
+    hsets = [(pinned_copy(x.routed), pinned_copy(x.shared)) for x, _, _ in b.sets[:n_host]]
     h_out = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
     h_ws = torch.empty(binding.latent_tail_host_workspace_size(P, T, L, H), dtype=torch.uint8,
                        device=dev)
