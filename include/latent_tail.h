@@ -146,6 +146,10 @@ LT_API lt_status latent_tail_norm(const uint16_t* routed, const float* norm_weig
  * Range rules as in latent_tail_forward_cols; results are bit-identical to the
  * projection step of latent_tail_forward given the same latent. With P = 1 this
  * is the per-rank compute after the reference's all-reduce.
+ * For T <= 128 the kernel is launched as a programmatic dependent of the work
+ * before it on the stream: it may start (set up its barriers and tensor memory)
+ * before that work has finished, but it reads no input and writes no output
+ * until that work is complete, so back-to-back calls overlap only set-up.
  */
 LT_API lt_status latent_tail_project_cols(const uint16_t* latent, const uint16_t* shared,
                                           const uint16_t* W, uint16_t* out, int P, int T,
