@@ -103,3 +103,51 @@ def test_side_stream_and_repeat_determinism():
     assert torch.equal(a, b)
     for _ in range(3):
         assert torch.equal(gh.run(x), a)
+
+
+@pytest.mark.parametrize("T", [64, 128, 256])
+def test_back_to_back_calls_read_what_the_previous_call_wrote(T):
+    """Each call's output is every input of the next one (P = 1, T = H = L: the
+    output [T, H] doubles as latent/routed [T, L], shared [1, T, H] and W [H, L]).
+    Issued back to back on one stream, the chain must give the same bits as the
+    same calls with a device synchronize between them: a call that started early
+    (programmatic dependent launch) must still read only after the previous call
+    has finished writing."""
+    torch.manual_seed(T)
+    H = L = T
+    eps = inputs.EPS
+    a0 = (torch.randn(T, H, device="cuda") / 8).to(torch.bfloat16)
+    g = (1.0 + 0.1 * torch.randn(L, device="cuda")).float()
+
+    def project_chain(sync):
+        bufs = [a0.clone()] + [torch.empty_like(a0) for _ in range(4)]
+        for i in range(4):
+            a = bufs[i]
+            binding.latent_tail_project_cols(a, a.view(1, T, H), a, bufs[i + 1], 0, H)
+            if sync:
+                torch.cuda.synchronize()
+        binding.latent_tail_check()
+        return bufs[1:]
+
+    def forward_chain(sync):
+        bufs = [a0.clone()] + [torch.empty_like(a0) for _ in range(4)]
+        ws = torch.empty(binding.latent_tail_workspace_size(1, T, L, H), dtype=torch.uint8,
+                         device="cuda")
+        for i in range(4):
+            a = bufs[i]
+            binding.latent_tail_forward(a.view(1, T, L), a.view(1, T, H), g, a, bufs[i + 1], eps,
+                                        ws)
+            if sync:
+                torch.cuda.synchronize()
+        binding.latent_tail_check()
+        return bufs[1:]
+
+    for chain in (project_chain, forward_chain):
+        free, synced = chain(False), chain(True)
+        for i, (u, v) in enumerate(zip(free, synced)):
+            assert torch.equal(u.view(torch.int16), v.view(torch.int16)), f"{chain.__name__} step {i}"
+    # and the first projection step against a float64 evaluation of its inputs
+    first = project_chain(True)[0]
+    a = a0.double()
+    want = a @ a.t() + a
+    torch.testing.assert_close(first.double(), want, atol=gh.ATOL, rtol=gh.RTOL)
