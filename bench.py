@@ -252,6 +252,21 @@ def job_throughput(tokens_per_rank_step, steps, world, seconds):
     return tokens_per_rank_step * steps * world / seconds
 
 
+def host_cpu_model():
+    """The host CPU's model name (Linux /proc/cpuinfo, else the platform string)."""
+    import platform
+
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                if key.strip() in ("model name", "Model name", "CPU part") and val.strip():
+                    return val.strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(w, budget_s=12.0, max_tokens=None):
     """The oracle as it stands, single-threaded, on a bounded sample of tokens
     of the same workload (drawn on the CPU with the workload's seed)."""
@@ -279,7 +294,7 @@ def cpu_baseline(w, budget_s=12.0, max_tokens=None):
     return {"value": done / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{reps} call(s) of {n} of the {w.T} tokens of the {w.name} workload "
                       f"(P={w.P}, L={w.L}, H={w.H}), FP32 single-threaded, {dt:.2f} s",
-            "host_cores": os.cpu_count()}
+            "host_cores": os.cpu_count(), "host_cpu": host_cpu_model()}
 
 
 def reference_arm(args):
