@@ -256,14 +256,19 @@ def host_cpu_model():
     """The host CPU's model name (Linux /proc/cpuinfo, else the platform string)."""
     import platform
 
+    part = None
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
                 key, _, val = line.partition(":")
-                if key.strip() in ("model name", "Model name", "CPU part") and val.strip():
+                if key.strip() in ("model name", "Model name") and val.strip():
                     return val.strip()
+                if key.strip() == "CPU part" and val.strip():
+                    part = val.strip()
     except OSError:
         pass
+    if part:  # Arm: no model name, only the part number (0xd4f is Neoverse V2)
+        return f"{platform.machine()} CPU part {part}"
     return platform.processor() or platform.machine()
 
 
