@@ -355,7 +355,7 @@ def reference_arm(args):
 
 # The other benchmark configurations, measured after the headline workload and
 # reported under "workloads" in the same line.
-SUB_WORKLOADS = ("decode", "decode_T1", "decode_T8", "decode_T32", "decode_T64",
+SUB_WORKLOADS = ("decode", "decode_T1", "decode_T2", "decode_T4", "decode_T8", "decode_T32", "decode_T64",
                  "decode_T128", "prefill", "prefill_p1")
 
 
@@ -365,7 +365,9 @@ def roofline_of(w, us_proj, us_call, hbm, tc_burst, peak_kind):
     peak than its bytes at the HBM peak (the P = 1 prefill)."""
     P, T, L, H = w.P, w.T, w.L, w.H
     pb, cb, fl = project_bytes(P, T, L, H), call_bytes(P, T, L, H), flops(T, L, H)
-    kname = "decode_kernel" if T <= 128 else "prefill_kernel"
+    # T <= 2 at these widths (one SM's W slice fits in shared memory): the
+    # one-launch CUDA-core kernel; up to 128 tokens the split-K decode kernel.
+    kname = "gemv_kernel" if T <= 2 else "decode_kernel" if T <= 128 else "prefill_kernel"
     proj_gbs = pb / (us_proj * 1e-6) / 1e9
     if fl / (tc_burst * 1e12) > pb / (hbm * 1e9):
         proj_tf = fl / (us_proj * 1e-6) / 1e12

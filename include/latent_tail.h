@@ -97,10 +97,14 @@ LT_API size_t latent_tail_workspace_size(int P, int T, int L, int H);
  *   workspace, workspace_bytes  at least latent_tail_workspace_size(P,T,L,H)
  *                               bytes of device scratch; its contents on entry
  *                               are ignored and on return are unspecified
- * Launches two kernels: reduce + RMSNorm into the workspace, then the
- * up-projection with the shared-partial epilogue (decode kernel for T <= 128,
- * persistent tensor-core kernel above), chained by programmatic dependent
- * launch. For T <= 128 the first kernel also prefetches routed and the W rows
+ * For T <= 2 (when L <= 4096 and one SM's share of W fits in its shared
+ * memory, e.g. L = 2048 at H = 7168) one CUDA-core kernel does the whole tail;
+ * the normalized latent then stays in FP32, unrounded, and the workspace is
+ * not used. Otherwise two kernels run: reduce + RMSNorm into the workspace
+ * (bf16), then the up-projection with the shared-partial epilogue (decode
+ * kernel for T <= 128, persistent tensor-core kernel above), chained by
+ * programmatic dependent launch. For 2 < T <= 128 the first kernel also
+ * prefetches routed and the W rows
  * into L2 before it waits for the preceding work on the stream (an L2
  * prefetch is only a hint: if that work is still writing routed, the lines are
  * updated in L2 and every read happens after the wait). Calls issued back to
@@ -206,9 +210,10 @@ LT_API lt_status latent_tail_forward_noalloc(const uint16_t* routed, const uint1
 
 /*
  * Bytes of device workspace latent_tail_forward_host needs: the normalized
- * latent as for latent_tail_workspace_size, plus, for T > 128, device staging
- * for routed, shared and out (each rounded up to 256 bytes). Returns 0 for
- * T <= 0 or invalid shapes. Host-only, never touches the GPU.
+ * latent as for latent_tail_workspace_size, plus device staging for routed when
+ * T <= 2, and for routed, shared and out when T > 128 (each rounded up to 256
+ * bytes). Returns 0 for T <= 0 or invalid shapes. Host-only, never touches the
+ * GPU.
  */
 LT_API size_t latent_tail_host_workspace_size(int P, int T, int L, int H);
 
@@ -228,8 +233,12 @@ LT_API size_t latent_tail_host_workspace_size(int P, int T, int L, int H);
  *     exactly one of the shared partials).
  *   workspace: latent_tail_host_workspace_size(P, T, L, H) bytes of device
  *     memory, not overlapping W or norm_weight.
- * For T <= 128 the kernels read the partials and write the result through the
- * host link directly: no staging copy, the host bytes cross the link once.
+ * When the one-launch kernel serves the shape (T <= 2, as for
+ * latent_tail_forward), a copy kernel first brings the routed partials into
+ * the workspace; the kernel then reads shared and writes out through the host
+ * link. Otherwise, for T <= 128, the kernels read the partials and write the
+ * result through the host link directly: no staging copy, the host bytes cross
+ * the link once.
  * Above, the partials are copied into the workspace (one cudaMemcpyAsync per
  * tensor), the device path runs, and the result is copied back. Like every
  * call it is asynchronous: out_host holds the result once `stream` has been

@@ -69,7 +69,7 @@ lt_status init_device(int dev, DeviceSlot& slot) {
     g_ptr_attr = reinterpret_cast<PointerGetAttributeFn>(fn);
   }
   if (lt::setup_norm(d) != cudaSuccess || lt::setup_decode(d) != cudaSuccess ||
-      lt::setup_prefill(d) != cudaSuccess)
+      lt::setup_prefill(d) != cudaSuccess || lt::setup_gemv(d) != cudaSuccess)
     return LT_ERR_CUDA;
   return LT_OK;
 }
@@ -168,7 +168,8 @@ lt_status run_project(const lt::ProjectArgs& a, const lt::DeviceInfo& dev, cudaS
 lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const float* g,
                        const uint16_t* W, uint16_t* out, int P, int T, int L, int H, float eps,
                        int c0, int c1, void* ws, size_t ws_bytes, lt_stream stream,
-                       bool early_trigger = true, bool routed_in_device_memory = true) {
+                       bool early_trigger = true, bool routed_in_device_memory = true,
+                       bool shared_on_host = false) {
   lt_status st = check_shape(P, T, L, H);
   if (st != LT_OK) return st;
   if ((st = check_range(H, c0, c1)) != LT_OK) return st;
@@ -193,6 +194,12 @@ lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const flo
   const lt::DeviceInfo* dev = nullptr;
   if ((st = current_device(&dev)) != LT_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (routed_in_device_memory && T <= lt::kGemvMaxTokens &&
+      lt::gemv_supported(T, L, c0, c1, *dev)) {  // the whole tail in one launch
+    const lt::GemvArgs ga{routed, g, nullptr, shared, W, out, P, T, L, H, c0, c1, eps,
+                          shared_on_host};
+    return launch_status(lt::launch_gemv(ga, *dev, s));
+  }
   uint16_t* y = static_cast<uint16_t*>(ws);
   lt::NormArgs na{routed, g, y, P, T, L, eps, nullptr, 0, false};
   if (T <= lt::kDecodeMaxTokens) {
@@ -261,6 +268,8 @@ LT_API lt_status latent_tail_forward_cols(const uint16_t* routed, const uint16_t
 LT_API size_t latent_tail_host_workspace_size(int P, int T, int L, int H) {
   if (T <= 0 || check_shape(P, T, L, H) != LT_OK) return 0;
   size_t b = round256(latent_bytes(T, L));
+  if (T <= lt::kGemvMaxTokens)  // staging for the routed partials (one-launch kernel)
+    b += round256(static_cast<size_t>(P) * T * L * 2);
   if (T > lt::kDecodeMaxTokens)  // staging for the partials and the result
     b += round256(static_cast<size_t>(P) * T * L * 2) + round256(static_cast<size_t>(P) * T * H * 2) +
          round256(static_cast<size_t>(T) * H * 2);
@@ -300,6 +309,18 @@ LT_API lt_status latent_tail_forward_host(const uint16_t* routed_host, const uin
   if (rd == nullptr || sd == nullptr || od == nullptr) return LT_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t y_bytes = round256(latent_bytes(T, L));
+  if (T <= lt::kGemvMaxTokens && lt::gemv_supported(T, L, 0, H, *dev)) {
+    // The one-launch kernel reads the routed partials once per CTA: a copy
+    // kernel brings them (P*T*L*2 bytes) into the workspace first; shared and
+    // out stay on the host link, read and written once. Same kernel, same bits
+    // as the device call.
+    uint16_t* r_st = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + y_bytes);
+    if (lt::launch_stage(rd, r_st, r_bytes, *dev, s) != cudaSuccess) return LT_ERR_CUDA;
+    return forward_impl(r_st, static_cast<const uint16_t*>(sd), norm_weight, W,
+                        static_cast<uint16_t*>(od), P, T, L, H, eps, 0, H, workspace, y_bytes,
+                        stream, /*early_trigger=*/true, /*routed_in_device_memory=*/true,
+                        /*shared_on_host=*/true);
+  }
   if (T <= lt::kDecodeMaxTokens) {
     // The kernels read the partials and write the result across the host link.
     // Here the host link, not the W stream, bounds a call, and releasing the
@@ -360,13 +381,19 @@ LT_API lt_status latent_tail_project_cols(const uint16_t* latent, const uint16_t
     return LT_ERR_INVALID_ARG;
   const lt::DeviceInfo* dev = nullptr;
   if ((st = current_device(&dev)) != LT_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T <= lt::kGemvMaxTokens && lt::gemv_supported(T, L, col_start, col_end, *dev)) {
+    const lt::GemvArgs ga{nullptr, nullptr, latent, shared, W, out, P, T, L, H,
+                          col_start, col_end, 0.f, false};
+    return launch_status(lt::launch_gemv(ga, *dev, s));
+  }
   // The decode kernel is launched as a programmatic dependent with every read
   // after its dependency wait: back-to-back calls overlap one launch's start-up
   // (barrier set-up, TMEM allocation) with the previous launch's tail.
   const bool dep = T <= lt::kDecodeMaxTokens;
   const lt::ProjectArgs pa{latent, shared, W, out, P,   T,   L,    H,
                            col_start, col_end, dep, dep, false};
-  return run_project(pa, *dev, reinterpret_cast<cudaStream_t>(stream));
+  return run_project(pa, *dev, s);
 }
 
 LT_API lt_status latent_tail_check(lt_stream stream) {

@@ -15,6 +15,11 @@ constexpr uint32_t kErrWaitTimeout = 1u;
 // the persistent tensor-core kernel runs.
 constexpr int kDecodeMaxTokens = 128;
 
+// Up to this many tokens a call runs the CUDA-core kernel that does the whole
+// tail in one launch (gemv.cu), when one SM's slice of W fits in its shared
+// memory and L <= 4096.
+constexpr int kGemvMaxTokens = 2;
+
 // Encodes a 2-D bf16 row-major [rows, cols] tensor map with a (64 x box_rows)
 // box and 128-byte swizzle, without L2 sector promotion: every box reads
 // 128-byte row pieces whose neighbours are read much later, if at all (see the
@@ -72,8 +77,32 @@ struct ProjectArgs {
   bool inputs_ready;
 };
 
+// The whole tail on CUDA cores for T <= kGemvMaxTokens. With latent == nullptr
+// the kernel reduces `routed` and normalizes it itself; otherwise it reads the
+// latent [T, L] (latent_tail_project_cols) and ignores routed, g and eps.
+struct GemvArgs {
+  const uint16_t* routed;  // [P,T,L]
+  const float* g;          // [L] or null (no norm)
+  const uint16_t* latent;  // [T,L] or null
+  const uint16_t* shared;  // [P,T,H]
+  const uint16_t* W;       // [H,L]
+  uint16_t* out;           // [T,H]
+  int P, T, L, H;
+  int col_start, col_end;
+  float eps;
+  bool shared_on_host;     // shared is mapped page-locked host memory: not prefetched
+};
+
 cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const DeviceInfo& dev,
                         cudaStream_t stream);
+cudaError_t launch_gemv(const GemvArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+// Copies `bytes` (a multiple of 16, both pointers 16-byte aligned) from mapped
+// page-locked host memory to device memory in a kernel launched as a
+// programmatic dependent (no copy-engine round trip on the stream).
+cudaError_t launch_stage(const void* src, void* dst, size_t bytes, const DeviceInfo& dev,
+                         cudaStream_t stream);
+// Whether launch_gemv serves this shape on this device (T and the W slice fit).
+bool gemv_supported(int T, int L, int col_start, int col_end, const DeviceInfo& dev);
 cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
@@ -84,5 +113,6 @@ cudaError_t launch_wait_probe(uint64_t limit_ns, const DeviceInfo& dev, cudaStre
 cudaError_t setup_norm(const DeviceInfo& dev);
 cudaError_t setup_decode(const DeviceInfo& dev);
 cudaError_t setup_prefill(const DeviceInfo& dev);
+cudaError_t setup_gemv(const DeviceInfo& dev);
 
 }  // namespace lt

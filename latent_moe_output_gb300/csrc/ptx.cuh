@@ -119,6 +119,17 @@ __device__ __forceinline__ void l2_prefetch_bulk(const void* src, uint32_t bytes
                ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes) : "memory");
 }
 
+// One-dimensional bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory; completion is signalled on `bar` as
+// transaction bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -382,6 +393,13 @@ __device__ __forceinline__ uint4 ld_l2_v4(const void* p) {
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
+  return v;
+}
+
+// 2-byte load served by L2 only (see ld_l2_v4).
+__device__ __forceinline__ uint16_t ld_l2_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p));
   return v;
 }
 

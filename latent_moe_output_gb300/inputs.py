@@ -49,7 +49,7 @@ TINY = Workload("tiny", P=2, T=5, L=64, H=128, seed=0)
 DECODE = Workload("decode", P=8, T=16, L=2048, H=7168, seed=1)
 DECODE_SWEEP = tuple(
     Workload(f"decode_T{t}", P=8, T=t, L=2048, H=7168, seed=1000 + t)
-    for t in (1, 8, 32, 64, 128)
+    for t in (1, 2, 4, 8, 32, 64, 128)
 )
 PREFILL = Workload("prefill", P=8, T=8192, L=2048, H=7168, seed=2)
 STRESS = Workload("stress", P=16, T=16384, L=2048, H=7168, seed=3, outlier_rows=True)

@@ -90,7 +90,7 @@ def test_workloads_are_the_benchmark_configurations():
     w = inputs.WORKLOADS
     assert (w["tiny"].P, w["tiny"].T, w["tiny"].L, w["tiny"].H, w["tiny"].seed) == (2, 5, 64, 128, 0)
     assert (w["decode"].P, w["decode"].T, w["decode"].L, w["decode"].H) == (8, 16, 2048, 7168)
-    assert sorted(x.T for x in inputs.DECODE_SWEEP) == [1, 8, 32, 64, 128]
+    assert sorted(x.T for x in inputs.DECODE_SWEEP) == [1, 2, 4, 8, 32, 64, 128]
     assert all(x.seed == 1000 + x.T and x.P == 8 for x in inputs.DECODE_SWEEP)
     assert (w["prefill"].P, w["prefill"].T) == (8, 8192)
     assert (w["stress"].P, w["stress"].T, w["stress"].outlier_rows) == (16, 16384, True)

@@ -42,6 +42,7 @@ def test_overlapping_output_is_rejected():
 
 
 @pytest.mark.parametrize("P,T,L,H,c0,c1", [
+    (3, 2, 2048, 7168, 0, 7168), (3, 2, 2048, 7168, 1000, 5000),   # one-launch kernel
     (3, 16, 512, 1024, 0, 1024), (3, 16, 512, 1024, 256, 512),     # decode kernel
     (3, 300, 512, 1024, 0, 1024), (3, 300, 512, 1024, 128, 896),   # prefill, 256-col tiles
     (3, 200, 512, 1024, 0, 1024), (3, 200, 512, 1024, 128, 896),   # prefill, 128-col tiles
@@ -151,3 +152,40 @@ def test_back_to_back_calls_read_what_the_previous_call_wrote(T):
     a = a0.double()
     want = a @ a.t() + a
     torch.testing.assert_close(first.double(), want, atol=gh.ATOL, rtol=gh.RTOL)
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_back_to_back_one_launch_calls_read_what_the_previous_call_wrote(T):
+    """The same property at T <= 2 (the one-launch kernel, which starts before
+    the previous kernel on the stream has finished): with H = L, each call writes
+    its [T, H] output into the first T rows of the next call's W, and that block
+    is also the next call's latent/routed and shared partial."""
+    torch.manual_seed(60 + T)
+    H = L = 1024
+    eps = inputs.EPS
+    w0 = (torch.randn(H, L, device="cuda") / 32).to(torch.bfloat16)
+    g = (1.0 + 0.1 * torch.randn(L, device="cuda")).float()
+
+    def chain(forward, sync):
+        Ws = [w0.clone() for _ in range(5)]
+        ws = torch.empty(binding.latent_tail_workspace_size(1, T, L, H), dtype=torch.uint8,
+                         device="cuda")
+        for i in range(4):
+            a, out = Ws[i][:T], Ws[i + 1][:T]
+            if forward:
+                binding.latent_tail_forward(a.view(1, T, L), a.view(1, T, H), g, Ws[i], out, eps,
+                                            ws)
+            else:
+                binding.latent_tail_project_cols(a, a.view(1, T, H), Ws[i], out, 0, H)
+            if sync:
+                torch.cuda.synchronize()
+        binding.latent_tail_check()
+        return [w[:T] for w in Ws[1:]]
+
+    for forward in (False, True):
+        free, synced = chain(forward, False), chain(forward, True)
+        for i, (u, v) in enumerate(zip(free, synced)):
+            assert torch.equal(u.view(torch.int16), v.view(torch.int16)), f"forward={forward} step {i}"
+    first = chain(False, True)[0].double()
+    a, w = w0[:T].double(), w0.double()
+    torch.testing.assert_close(first, a @ w.t() + a, atol=gh.ATOL, rtol=gh.RTOL)

@@ -52,8 +52,13 @@ def test_decode_sweep(w):
     (1, 1000, 64, 2056),   # many tiles, one K-block, P = 1 (pre-reduced latent)
     (16, 200, 256, 264),   # P = 16 partials
     (64, 4, 256, 256),     # P = 64, the largest partial count accepted (decode)
+    (64, 2, 256, 256),     # P = 64 on the one-launch kernel
     (64, 200, 128, 256),   # P = 64 on the prefill path
     (2, 8, 16384, 256),    # L = 16384, the largest latent width accepted (decode)
+    (2, 2, 4096, 256),     # T = 2 at L = 4096: the widest latent the one-launch kernel takes
+    (2, 2, 8192, 256),     # T = 2 at L = 8192: too wide for it, the two-kernel path runs
+    (3, 2, 2048, 19464),   # T = 2, one SM's W slice too large: the two-kernel path runs
+    (3, 2, 328, 1000),     # one-launch kernel, ragged latent (328 = 256 + 72)
     (2, 260, 16384, 128),  # L = 16384 on the prefill path
     (1, 3, 8, 8),          # L = H = 8, the smallest accepted: boxes wider than the tensor
     (2, 130, 8, 16),       # the same on the prefill path
@@ -75,6 +80,29 @@ def test_full_size_every_element(w):
     gh.assert_parity(got, want, w.name)
     if w.outlier_rows:  # the outlier rows are among the rows compared above
         assert len(x.scaled_up) == len(x.scaled_down) == w.T // 100
+
+
+@pytest.mark.parametrize("T", [1, 2, 3])
+def test_one_launch_token_counts(T):
+    """T <= 2 at the production widths (P = 8, L = 2048, H = 7168): the CUDA-core
+    kernel that does the whole tail in one launch, every element; T = 3 is the
+    first token count of the two-kernel path."""
+    check_full(inputs.make(8, T, 2048, 7168, seed=900 + T), what=f"one-launch T{T}")
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_one_launch_column_ranges_tile_the_full_call(T):
+    """Column ranges that tile [0, H) reproduce the full call bit for bit: each
+    output element is formed by one warp in the same order whatever the range,
+    and every CTA builds the same FP32 latent. The ranges have different widths,
+    so each gives its CTAs a different number of W rows."""
+    assert T <= 2  # the one-launch kernel
+    x = gh.to_dev(inputs.make(8, T, 2048, 7168, seed=950 + T))
+    full = gh.run(x)
+    pieces = torch.full_like(full, float("nan"))
+    for c0, c1 in ((0, 1000), (1000, 4104), (4104, 7160), (7160, 7168)):
+        gh.run(x, c0, c1, out=pieces)
+    assert torch.equal(pieces.view(torch.int16), full.view(torch.int16))
 
 
 def test_norm_stage_matches_oracle_latent():
@@ -111,7 +139,7 @@ def test_zero_tokens():
     binding.latent_tail_check()
 
 
-@pytest.mark.parametrize("P,T,L,H", [(2, 5, 64, 128), (8, 16, 2048, 7168), (3, 300, 328, 1000),
+@pytest.mark.parametrize("P,T,L,H", [(2, 5, 64, 128), (8, 2, 2048, 7168), (8, 16, 2048, 7168), (3, 300, 328, 1000),
                                      (2, 200, 256, 1000)])
 def test_no_norm_branch(P, T, L, H):
     """norm_weight = None: the latent is the routed partial sum itself (the

@@ -43,7 +43,8 @@ def test_noalloc_matches_forward_on_calls_in_a_row():
     stream = torch.cuda.current_stream()
     # T = 2048 at L = 2048 needs exactly the whole array (prefill kernel); the
     # decode-sized calls after it read only the first rows of what it left.
-    shapes = [(8, 2048, 2048, 7168, 41), (8, 16, 2048, 7168, 42), (8, 128, 2048, 7168, 43)]
+    shapes = [(8, 2048, 2048, 7168, 41), (8, 16, 2048, 7168, 42), (8, 128, 2048, 7168, 43),
+              (8, 1, 2048, 7168, 44)]
     assert binding.latent_tail_workspace_size(8, 2048, 2048, 7168) == MAX_SCRATCH
     for P, T, L, H, seed in shapes:
         x = inputs.make(P, T, L, H, seed=seed)
