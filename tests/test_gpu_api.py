@@ -30,7 +30,8 @@ def test_small_workspace_is_rejected_and_nothing_runs():
 
 def test_overlapping_output_is_rejected():
     x = gh.to_dev(inputs.make(2, 16, 256, 256, seed=2))
-    ws = torch.empty(16 * 256 * 2, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(binding.latent_tail_workspace_size(2, 16, 256, 256), dtype=torch.uint8,
+                     device="cuda")
     flat = x.shared.view(-1)
     straddle = flat[8 * 256: 8 * 256 + 16 * 256].view(16, 256)  # half in each partial
     with pytest.raises(LatentTailError) as e:
@@ -106,7 +107,7 @@ def test_side_stream_and_repeat_determinism():
         assert torch.equal(gh.run(x), a)
 
 
-@pytest.mark.parametrize("T", [64, 128, 256])
+@pytest.mark.parametrize("T", [16, 64, 128, 256])
 def test_back_to_back_calls_read_what_the_previous_call_wrote(T):
     """Each call's output is every input of the next one (P = 1, T = H = L: the
     output [T, H] doubles as latent/routed [T, L], shared [1, T, H] and W [H, L]).

@@ -59,6 +59,9 @@ def test_decode_sweep(w):
     (2, 2, 8192, 256),     # T = 2 at L = 8192: too wide for it, the two-kernel path runs
     (3, 2, 2048, 19464),   # T = 2, one SM's W slice too large: the two-kernel path runs
     (3, 2, 328, 1000),     # one-launch kernel, ragged latent (328 = 256 + 72)
+    (1, 1, 8, 8),          # L = H = 8 on the one-launch kernel: one CTA, one 8-row chunk
+    (7, 1, 2056, 7176),    # one-launch: 257 latent pieces (two for thread 0), P = 7, last CTA 24 rows
+    (9, 2, 4096, 1024),    # one-launch: the widest latent (two pieces per thread), P = 9 (two batches)
     (2, 260, 16384, 128),  # L = 16384 on the prefill path
     (1, 3, 8, 8),          # L = H = 8, the smallest accepted: boxes wider than the tensor
     (2, 130, 8, 16),       # the same on the prefill path
