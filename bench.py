@@ -18,7 +18,7 @@ used.
 
 The line also carries, under "workloads", µs/call, tokens/s, the roofline of
 the dominant kernel and the single-call latency of every other benchmark
-configuration (decode P8 T16, the decode sweep T = 1..128, prefill P8 T8192 and
+configuration (decode P8 T16, the decode sweep T = 1, 2, 4, 8, 32, 64, 128, prefill P8 T8192 and
 the pre-reduced P=1 prefill).
 
 `single_call_us_median` is the median device time of one call with nothing else
