@@ -396,13 +396,6 @@ __device__ __forceinline__ uint4 ld_l2_v4(const void* p) {
   return v;
 }
 
-// 2-byte load served by L2 only (see ld_l2_v4).
-__device__ __forceinline__ uint16_t ld_l2_u16(const void* p) {
-  uint16_t v;
-  asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p));
-  return v;
-}
-
 // 16-byte store marked streaming (evict first): output that is written once and
 // not read again by this kernel, so it does not displace re-read operands in L2.
 __device__ __forceinline__ void st_stream_v4(void* p, const uint4& v) {
