@@ -22,11 +22,12 @@
 //     prefetches its W while this call finishes;
 //   * while W streams in, the epilogue warps sum the P shared partials of the
 //     rows this CTA finishes (p ascending, FP32) into shared memory;
-//   * after the MMAs, every CTA pushes each accumulator row into the shared
-//     memory of the cluster CTA that finishes that row (DSMEM stores), one
-//     cluster barrier, then each CTA adds the KS partials in fixed slice order
-//     plus the shared sum and stores bf16. The summation order never depends
-//     on the requested column range.
+//   * after the MMAs and a cluster barrier (every stage ring of the cluster is
+//     then free), every CTA pushes each accumulator row into the ring of the
+//     cluster CTA that finishes that row (DSMEM stores, token-major so that a
+//     warp's stores are contiguous), a second cluster barrier, then each CTA
+//     adds the KS partials in fixed slice order plus the shared sum and stores
+//     bf16. The summation order never depends on the requested column range.
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -57,8 +58,8 @@ struct DecodeParams {
   int npad;        // MMA N: tokens rounded up to a multiple of 16
   int stages;
   int tmem_cols;
-  uint32_t ssum_offset;  // byte offsets (from the 1024-aligned base) of the
-  uint32_t slot_offset;  // shared-partial sums and of the received K-slice partials
+  uint32_t ssum_offset;  // byte offsets (from the 1024-aligned base) of the shared-partial
+  uint32_t slot_offset;  // sums and of the received K-slice partials (0: in the ring)
   int pdl;
   int inputs_ready;         // W and shared complete at launch (only y is awaited)
   int trigger_after_issue;  // allow dependents once the last W copy is issued
@@ -84,9 +85,12 @@ __device__ __forceinline__ void add8(float (&a)[8], const uint4& v) {
 }
 
 // Shared-memory layout from the 1024-aligned base:
-//   [0, ring)          stage ring: W box [128 x 64] then y box [npad x 64], 128B swizzle
+//   [0, region)        stage ring: W box [128 x 64] then y box [npad x 64], 128B swizzle
 //   [ssum_offset, ..)  ssum[t][r]: sum_p shared[p, t, h0 + r0 + r] for this CTA's rows
-//   [slot_offset, ..)  slot[src][r][t]: K-slice partial of row r0 + r pushed by CTA src
+//   [slot_offset, ..)  slot[src][t][r]: the K-slice partial of row r0 + r pushed by CTA
+//                      src; above 32 tokens slot_offset is 0: the partials then reuse
+//                      the ring once every CTA of the cluster has finished its MMAs,
+//                      which leaves room for more stages (region = the larger of the two)
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap w_map,
                   const __grid_constant__ CUtensorMap y_map, const DecodeParams p) {
@@ -140,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const bool have_acc = nkb > 0;
+  bool acc_ok = true;  // epilogue warps: the accumulator is complete and readable
 
   if (warp == 0) {
     if (lane == 0 && nkb > 0) {
@@ -225,66 +230,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       dst[0] = make_float4(a[0], a[1], a[2], a[3]);
       dst[1] = make_float4(a[4], a[5], a[6], a[7]);
     }
-    // (b) Accumulator rows -> the shared memory of the CTA that finishes them
-    //     (distributed shared memory stores into its slot[rank]).
-    bool ok = true;
+    // (b) Wait for this CTA's MMAs (its ring is then no longer read).
     if (have_acc) {
-      ok = mbar_wait(smem_u32(&acc_bar), 0, p.err, abort_v);
+      acc_ok = mbar_wait(smem_u32(&acc_bar), 0, p.err, abort_v);
       tc_fence_after();
     }
-    ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below needs a converged warp
+    acc_ok = __all_sync(0xffffffffu, acc_ok);  // tcgen05.ld below needs a converged warp
     if (lane == 0 && warp == 2 && !p.trigger_after_issue)
       pdl_launch_dependents();  // the next call may start its prologue
+  }
+  if (p.slot_offset == 0) {  // the same for every CTA of the launch
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();  // every CTA of the cluster is past its MMAs: its ring may take the partials
+    tc_fence_after();
+  }
+
+  // (c) Accumulator rows -> the shared memory of the CTA that finishes them
+  //     (distributed shared memory stores into its slot[rank]). The lanes of a
+  //     warp hold consecutive rows, which slot keeps adjacent for each token, so
+  //     every store of the warp fills one contiguous 128-byte line.
+  if (warp >= 2) {
     const int q = warp & 3;            // TMEM lane quadrant of this warp
     const int row = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const int owner = row / rpc;
     const uint32_t dst_row = smem_u32(slot) +
-        static_cast<uint32_t>(((static_cast<int>(rank) * rpc + (row - owner * rpc)) * p.npad) * 4);
+        static_cast<uint32_t>((static_cast<int>(rank) * p.npad * rpc + (row - owner * rpc)) * 4);
     const uint32_t dsm = map_to_rank(dst_row, static_cast<uint32_t>(owner));
+    const uint32_t token_stride = static_cast<uint32_t>(rpc) * 4u;
     for (int c = 0; c < p.npad; c += 16) {
       float v[16];
       __syncwarp();
-      if (have_acc && ok) {
+      if (have_acc && acc_ok) {
         tmem_ld16(tmem + lane_base + static_cast<uint32_t>(c), v);
       } else {
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = 0.f;
       }
 #pragma unroll
-      for (int j = 0; j < 16; j += 4)
-        st_dsmem_f32x4(dsm + static_cast<uint32_t>((c + j) * 4), v[j], v[j + 1], v[j + 2],
-                       v[j + 3]);
+      for (int j = 0; j < 16; ++j)
+        st_dsmem_f32(dsm + static_cast<uint32_t>(c + j) * token_stride, v[j]);
     }
   }
   __syncwarp();
   cluster_sync();  // all K-slice partials of this CTA's rows have arrived
 
-  // (c) Finish this CTA's rows: K-slice partials summed in fixed order
-  //     (slice 0..KS-1), plus the shared-partial sum, rounded to bf16.
+  // (d) Finish this CTA's rows: K-slice partials summed in fixed order
+  //     (slice 0..KS-1), plus the shared-partial sum, rounded to bf16. A thread
+  //     keeps 4 consecutive rows (quads = rpc / 4 divides the 192 threads) and
+  //     takes every tstep-th token, four tokens' loads at a time; the lanes of
+  //     a warp read consecutive 16-byte pieces of slot and ssum.
   {
-    const int items = p.T * groups;
-    for (int i = threadIdx.x; i < items; i += kThreads) {
-      const int t = i / groups;
-      const int g = i - t * groups;
-      const int h = h0 + r0 + g * 8;
-      if (h < p.col_start || h >= p.col_end) continue;
-      float acc[8];
+    const int quads = rpc / 4;
+    const int g = static_cast<int>(threadIdx.x) % quads;
+    const int tstep = kThreads / quads;
+    const int h = h0 + r0 + g * 4;
+    if (h >= p.col_start && h < p.col_end) {  // ranges are multiples of 8
+      for (int t0 = static_cast<int>(threadIdx.x) / quads; t0 < p.T; t0 += 4 * tstep) {
+        float4 v[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-      for (int src = 0; src < p.ks; ++src) {
-        const float* sp = slot + (src * rpc + g * 8) * p.npad + t;
+        for (int u = 0; u < 4; ++u) {
+          const int t = t0 + u * tstep;
+          if (t >= p.T) break;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int src = 0; src < p.ks; ++src) {
+            const float4 a =
+                *reinterpret_cast<const float4*>(slot + (src * p.npad + t) * rpc + g * 4);
+            acc.x += a.x;
+            acc.y += a.y;
+            acc.z += a.z;
+            acc.w += a.w;
+          }
+          const float4 s = *reinterpret_cast<const float4*>(ssum + t * rpc + g * 4);
+          v[u] = make_float4(acc.x + s.x, acc.y + s.y, acc.z + s.z, acc.w + s.w);
+        }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] += sp[j * p.npad];
+        for (int u = 0; u < 4; ++u) {
+          const int t = t0 + u * tstep;
+          if (t >= p.T) break;
+          st_global_v2(p.out + static_cast<size_t>(t) * p.H + h, pack_bf16x2(v[u].x, v[u].y),
+                       pack_bf16x2(v[u].z, v[u].w));
+        }
       }
-      const float4* sp = reinterpret_cast<const float4*>(ssum + t * rpc + g * 8);
-      const float4 s0 = sp[0], s1 = sp[1];
-      uint4 o;
-      o.x = pack_bf16x2(acc[0] + s0.x, acc[1] + s0.y);
-      o.y = pack_bf16x2(acc[2] + s0.z, acc[3] + s0.w);
-      o.z = pack_bf16x2(acc[4] + s1.x, acc[5] + s1.y);
-      o.w = pack_bf16x2(acc[6] + s1.z, acc[7] + s1.w);
-      *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(t) * p.H + h) = o;
     }
   }
 
@@ -330,39 +358,46 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
   // Four slices (224 CTAs at H = 7168, two per SM) when their buffers fit in
   // half an SM's shared memory, else two (112 CTAs, one per SM), else one.
   const uint32_t stage_bytes = kWStageBytes + static_cast<uint32_t>(p.npad) * 128u;
-  // bytes of the shared-partial sums plus the received partials for `cand` slices
-  auto extra_bytes = [&](int cand) {
-    const int rpc = kBlockM / cand;
-    const size_t ss = (static_cast<size_t>(p.npad) * rpc * 4 + 1023) & ~size_t(1023);
-    const size_t sl = (static_cast<size_t>(cand) * rpc * p.npad * 4 + 1023) & ~size_t(1023);
-    return ss + sl;
+  // The received K-slice partials take 128 rows x npad FP32 whatever the split.
+  // Above 32 tokens they reuse the ring (one more cluster barrier, more stages:
+  // the region is then the larger of the two), else they have their own bytes.
+  const bool in_ring = p.npad > 32;
+  const size_t sl = (static_cast<size_t>(kBlockM) * p.npad * 4 + 1023) & ~size_t(1023);
+  auto ss_bytes = [&](int cand) {
+    return (static_cast<size_t>(p.npad) * (kBlockM / cand) * 4 + 1023) & ~size_t(1023);
   };
+  auto region_for = [&](long st) {
+    const size_t ring = static_cast<size_t>(st) * stage_bytes;
+    return in_ring ? std::max(ring, sl) : ring;
+  };
+  auto smem_for = [&](int cand, long st) {
+    return 1024 + region_for(st) + ss_bytes(cand) + (in_ring ? 0 : sl);
+  };
+  const long fixed_extra = in_ring ? 0 : static_cast<long>(sl);
   int ks = 1;
   int stages = 1;
   for (int cand : {4, 2}) {
     if (p.total_kb < 4 * cand) continue;  // at least 4 K-blocks per slice
     const long budget = cand == 4 ? kHalfSmBudget : kSmemBudget;
-    long st = (budget - 1024 - static_cast<long>(extra_bytes(cand))) /
+    long st = (budget - 1024 - static_cast<long>(ss_bytes(cand)) - fixed_extra) /
               static_cast<long>(stage_bytes);
     st = std::min<long>({st, ceil_div(p.total_kb, cand), kMaxStages});
-    if (st < (cand == 4 ? 3 : 2)) continue;
+    if (st < (cand == 4 ? 3 : 2) || smem_for(cand, st) > static_cast<size_t>(budget)) continue;
     ks = cand;
     stages = static_cast<int>(st);
     break;
   }
   if (ks == 1) {
-    const long st = (kSmemBudget - 1024 - static_cast<long>(extra_bytes(1))) /
+    const long st = (kSmemBudget - 1024 - static_cast<long>(ss_bytes(1)) - fixed_extra) /
                     static_cast<long>(stage_bytes);
     stages = static_cast<int>(std::max<long>(1, std::min<long>({st, p.total_kb, kMaxStages})));
   }
-  const size_t ring = static_cast<size_t>(stages) * stage_bytes;
+  const size_t region = region_for(stages);
   p.ks = ks;
   p.kb_per_cta = ceil_div(p.total_kb, ks);
   p.stages = stages;
-  const int rpc = kBlockM / ks;
-  p.ssum_offset = static_cast<uint32_t>(ring);
-  p.slot_offset = static_cast<uint32_t>(
-      ring + ((static_cast<size_t>(p.npad) * rpc * 4 + 1023) & ~size_t(1023)));
+  p.ssum_offset = static_cast<uint32_t>(region);
+  p.slot_offset = in_ring ? 0u : static_cast<uint32_t>(region + ss_bytes(ks));
   p.tmem_cols = next_pow2_at_least(p.npad, 32);
   p.pdl = a.pdl ? 1 : 0;
   p.inputs_ready = a.inputs_ready ? 1 : 0;
@@ -372,7 +407,7 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
   const int tile_last = (a.col_end - 1) / kBlockM;
   p.tile0 = tile_first;
   const int ntiles = tile_last - tile_first + 1;
-  const size_t smem = 1024 + ring + extra_bytes(ks);
+  const size_t smem = smem_for(ks, stages);
   if (smem > static_cast<size_t>(kSmemLimit)) return cudaErrorInvalidConfiguration;
 
   CUtensorMap w_map, y_map;
