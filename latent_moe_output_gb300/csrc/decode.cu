@@ -91,6 +91,8 @@ __device__ __forceinline__ void add8(float (&a)[8], const uint4& v) {
 //                      src; above 32 tokens slot_offset is 0: the partials then reuse
 //                      the ring once every CTA of the cluster has finished its MMAs,
 //                      which leaves room for more stages (region = the larger of the two)
+// kOnePerSm: the launch has one CTA per SM (KS <= 2); see (a) below.
+template <bool kOnePerSm>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap w_map,
                   const __grid_constant__ CUtensorMap y_map, const DecodeParams p) {
@@ -209,26 +211,76 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = threadIdx.x - 64;
     const size_t plane = static_cast<size_t>(p.T) * p.H;
     const int items = p.T * groups;
-    for (int i = et; i < items; i += kEpiThreads) {
-      const int t = i / groups;
-      const int g = i - t * groups;
-      const int h = h0 + r0 + g * 8;
-      float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (h >= p.col_start && h < p.col_end) {
-        const uint16_t* src = p.shared + static_cast<size_t>(t) * p.H + h;
+    if constexpr (kOnePerSm) {
+      // With one CTA per SM this sum can outlast the MMAs, so a thread takes two
+      // 8-column pieces at a time (16 loads in flight). With two CTAs per SM the
+      // extra loads and registers cost more than they saved (the loop below).
+      constexpr int per = 2;
+      for (int i0 = et; i0 < items; i0 += per * kEpiThreads) {
+        const uint16_t* src[2];
+        bool live[2], load[2];
+        float a[2][8];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i = i0 + u * kEpiThreads;
+          const int t = i / groups;
+          const int h = h0 + r0 + (i - t * groups) * 8;
+          live[u] = i < items;
+          load[u] = live[u] && h >= p.col_start && h < p.col_end;
+          src[u] = p.shared + static_cast<size_t>(t) * p.H + h;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) a[u][j] = 0.f;
+        }
         int pp = 0;
         for (; pp + 8 <= p.P; pp += 8) {
-          uint4 v[8];
+          uint4 v[2][8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) v[k] = ld_l2_v4(src + (pp + k) * plane);
+          for (int u = 0; u < 2; ++u)
+            if (load[u])
 #pragma unroll
-          for (int k = 0; k < 8; ++k) add8(a, v[k]);
+              for (int k = 0; k < 8; ++k) v[u][k] = ld_l2_v4(src[u] + (pp + k) * plane);
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (load[u])
+#pragma unroll
+              for (int k = 0; k < 8; ++k) add8(a[u], v[u][k]);
         }
-        for (; pp < p.P; ++pp) add8(a, ld_l2_v4(src + pp * plane));
+        for (; pp < p.P; ++pp)
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (load[u]) add8(a[u], ld_l2_v4(src[u] + pp * plane));
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (!live[u]) continue;
+          const int i = i0 + u * kEpiThreads;
+          const int t = i / groups;
+          float4* dst = reinterpret_cast<float4*>(ssum + t * rpc + (i - t * groups) * 8);
+          dst[0] = make_float4(a[u][0], a[u][1], a[u][2], a[u][3]);
+          dst[1] = make_float4(a[u][4], a[u][5], a[u][6], a[u][7]);
+        }
       }
-      float4* dst = reinterpret_cast<float4*>(ssum + t * rpc + g * 8);
-      dst[0] = make_float4(a[0], a[1], a[2], a[3]);
-      dst[1] = make_float4(a[4], a[5], a[6], a[7]);
+    } else {
+      for (int i = et; i < items; i += kEpiThreads) {
+        const int t = i / groups;
+        const int g = i - t * groups;
+        const int h = h0 + r0 + g * 8;
+        float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (h >= p.col_start && h < p.col_end) {
+          const uint16_t* src = p.shared + static_cast<size_t>(t) * p.H + h;
+          int pp = 0;
+          for (; pp + 8 <= p.P; pp += 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = ld_l2_v4(src + (pp + k) * plane);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) add8(a, v[k]);
+          }
+          for (; pp < p.P; ++pp) add8(a, ld_l2_v4(src + pp * plane));
+        }
+        float4* dst = reinterpret_cast<float4*>(ssum + t * rpc + g * 8);
+        dst[0] = make_float4(a[0], a[1], a[2], a[3]);
+        dst[1] = make_float4(a[4], a[5], a[6], a[7]);
+      }
     }
     // (b) Wait for this CTA's MMAs (its ring is then no longer read).
     if (have_acc) {
@@ -337,8 +389,13 @@ int next_pow2_at_least(int v, int lo) {
 }  // namespace
 
 cudaError_t setup_decode(const DeviceInfo&) {
-  return cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemLimit);
+  for (const void* f : {reinterpret_cast<const void*>(decode_kernel<false>),
+                        reinterpret_cast<const void*>(decode_kernel<true>)}) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
@@ -434,7 +491,8 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
   }
   cfg.attrs = attrs;
   cfg.numAttrs = static_cast<unsigned>(n);
-  return cudaLaunchKernelEx(&cfg, decode_kernel, w_map, y_map, p);
+  return ks <= 2 ? cudaLaunchKernelEx(&cfg, decode_kernel<true>, w_map, y_map, p)
+                 : cudaLaunchKernelEx(&cfg, decode_kernel<false>, w_map, y_map, p);
 }
 
 }  // namespace lt
