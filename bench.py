@@ -367,7 +367,8 @@ def roofline_of(w, us_proj, us_call, hbm, tc_burst, peak_kind):
     pb, cb, fl = project_bytes(P, T, L, H), call_bytes(P, T, L, H), flops(T, L, H)
     # T <= 2 at these widths (one SM's W slice fits in shared memory): the
     # one-launch CUDA-core kernel; up to 128 tokens the split-K decode kernel.
-    kname = "gemv_kernel" if T <= 2 else "decode_kernel" if T <= 128 else "prefill_kernel"
+    # which kernel a call runs at the bench's latent width (L = 2048)
+    kname = "gemv_kernel" if T <= 2 else "decode_kernel" if T <= 224 else "prefill_kernel"
     proj_gbs = pb / (us_proj * 1e-6) / 1e9
     if fl / (tc_burst * 1e12) > pb / (hbm * 1e9):
         proj_tf = fl / (us_proj * 1e-6) / 1e12

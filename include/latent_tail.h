@@ -102,9 +102,10 @@ LT_API size_t latent_tail_workspace_size(int P, int T, int L, int H);
  * the normalized latent then stays in FP32, unrounded, and the workspace is
  * not used. Otherwise two kernels run: reduce + RMSNorm into the workspace
  * (bf16), then the up-projection with the shared-partial epilogue (decode
- * kernel for T <= 128, persistent tensor-core kernel above), chained by
- * programmatic dependent launch. For 2 < T <= 128 the first kernel also
- * prefetches routed and the W rows
+ * kernel for T <= 224 when its buffers fit in shared memory, which they always
+ * do for T <= 128 and do at L = 2048; persistent tensor-core kernel otherwise),
+ * chained by programmatic dependent launch. When the decode kernel runs (and
+ * T > 2) the first kernel also prefetches routed and the W rows
  * into L2 before it waits for the preceding work on the stream (an L2
  * prefetch is only a hint: if that work is still writing routed, the lines are
  * updated in L2 and every read happens after the wait). Calls issued back to
@@ -150,7 +151,8 @@ LT_API lt_status latent_tail_norm(const uint16_t* routed, const float* norm_weig
  * Range rules as in latent_tail_forward_cols; results are bit-identical to the
  * projection step of latent_tail_forward given the same latent. With P = 1 this
  * is the per-rank compute after the reference's all-reduce.
- * For T <= 128 the kernel is launched as a programmatic dependent of the work
+ * When the decode kernel serves the call (see latent_tail_forward) it is
+ * launched as a programmatic dependent of the work
  * before it on the stream: it may start (set up its barriers and tensor memory)
  * before that work has finished, but it reads no input and writes no output
  * until that work is complete, so back-to-back calls overlap only set-up.
@@ -211,9 +213,10 @@ LT_API lt_status latent_tail_forward_noalloc(const uint16_t* routed, const uint1
 /*
  * Bytes of device workspace latent_tail_forward_host needs: the normalized
  * latent as for latent_tail_workspace_size, plus device staging for routed when
- * T <= 2, and for routed, shared and out when T > 128 (each rounded up to 256
- * bytes). Returns 0 for T <= 0 or invalid shapes. Host-only, never touches the
- * GPU.
+ * T <= 2, and for routed, shared and out when the call runs the persistent
+ * tensor-core kernel (above 224 tokens, or above 128 when the decode kernel's
+ * buffers do not fit; see latent_tail_forward), each rounded up to 256 bytes.
+ * Returns 0 for T <= 0 or invalid shapes. Host-only, never touches the GPU.
  */
 LT_API size_t latent_tail_host_workspace_size(int P, int T, int L, int H);
 
@@ -236,10 +239,10 @@ LT_API size_t latent_tail_host_workspace_size(int P, int T, int L, int H);
  * When the one-launch kernel serves the shape (T <= 2, as for
  * latent_tail_forward), a copy kernel first brings the routed partials into
  * the workspace; the kernel then reads shared and writes out through the host
- * link. Otherwise, for T <= 128, the kernels read the partials and write the
- * result through the host link directly: no staging copy, the host bytes cross
- * the link once.
- * Above, the partials are copied into the workspace (one cudaMemcpyAsync per
+ * link. Otherwise, when the decode kernel serves the call, the kernels read the
+ * partials and write the result through the host link directly: no staging
+ * copy, the host bytes cross the link once.
+ * For the persistent kernel the partials are copied into the workspace (one cudaMemcpyAsync per
  * tensor), the device path runs, and the result is copied back. Like every
  * call it is asynchronous: out_host holds the result once `stream` has been
  * synchronized, and the host buffers must not be modified before then.

@@ -160,8 +160,12 @@ size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
 lt_status launch_status(cudaError_t e) { return e == cudaSuccess ? LT_OK : LT_ERR_CUDA; }
 
+// Whether a call of T tokens at latent width L runs the decode kernel (else the
+// prefill kernel).
+bool decode_path(int T, int L) { return lt::decode_supported(T, L); }
+
 lt_status run_project(const lt::ProjectArgs& a, const lt::DeviceInfo& dev, cudaStream_t s) {
-  if (a.T <= lt::kDecodeMaxTokens) return launch_status(lt::launch_decode(a, dev, s));
+  if (decode_path(a.T, a.L)) return launch_status(lt::launch_decode(a, dev, s));
   return launch_status(lt::launch_prefill(a, dev, s));
 }
 
@@ -202,7 +206,7 @@ lt_status forward_impl(const uint16_t* routed, const uint16_t* shared, const flo
   }
   uint16_t* y = static_cast<uint16_t*>(ws);
   lt::NormArgs na{routed, g, y, P, T, L, eps, nullptr, 0, false};
-  if (T <= lt::kDecodeMaxTokens) {
+  if (decode_path(T, L)) {
     // The decode kernel streams W in whole 128-row tiles covering [c0, c1).
     const int r0 = c0 / lt::kDecodeTileRows * lt::kDecodeTileRows;
     const int r1 = std::min(H, (c1 + lt::kDecodeTileRows - 1) / lt::kDecodeTileRows *
@@ -270,7 +274,7 @@ LT_API size_t latent_tail_host_workspace_size(int P, int T, int L, int H) {
   size_t b = round256(latent_bytes(T, L));
   if (T <= lt::kGemvMaxTokens)  // staging for the routed partials (one-launch kernel)
     b += round256(static_cast<size_t>(P) * T * L * 2);
-  if (T > lt::kDecodeMaxTokens)  // staging for the partials and the result
+  if (!decode_path(T, L))  // prefill kernel: staging for the partials and the result
     b += round256(static_cast<size_t>(P) * T * L * 2) + round256(static_cast<size_t>(P) * T * H * 2) +
          round256(static_cast<size_t>(T) * H * 2);
   return b;
@@ -321,7 +325,7 @@ LT_API lt_status latent_tail_forward_host(const uint16_t* routed_host, const uin
                         stream, /*early_trigger=*/true, /*routed_in_device_memory=*/true,
                         /*shared_on_host=*/true);
   }
-  if (T <= lt::kDecodeMaxTokens) {
+  if (decode_path(T, L)) {
     // The kernels read the partials and write the result across the host link.
     // Here the host link, not the W stream, bounds a call, and releasing the
     // next call only after the MMAs measured faster than the early release.
@@ -390,7 +394,7 @@ LT_API lt_status latent_tail_project_cols(const uint16_t* latent, const uint16_t
   // The decode kernel is launched as a programmatic dependent with every read
   // after its dependency wait: back-to-back calls overlap one launch's start-up
   // (barrier set-up, TMEM allocation) with the previous launch's tail.
-  const bool dep = T <= lt::kDecodeMaxTokens;
+  const bool dep = decode_path(T, L);
   const lt::ProjectArgs pa{latent, shared, W, out, P,   T,   L,    H,
                            col_start, col_end, dep, dep, false};
   return run_project(pa, *dev, s);

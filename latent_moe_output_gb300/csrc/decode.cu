@@ -1,4 +1,4 @@
-// Steps 3-5 of the latent-MoE tail for decode-sized token counts (T <= 128):
+// Steps 3-5 of the latent-MoE tail for decode-sized token counts (T <= 224):
 //   out[t,h] = bf16_rn( sum_l y[t,l] * W[h,l] + sum_p shared[p,t,h] ),  h in [c0,c1)
 // The narrowed beta-add GEMM of PR #50383's `_shard_up_proj_tail`
 // (`hidden_shard.addmm_(latent, up_proj_shard.t())`) with the shared-partial
@@ -386,42 +386,29 @@ int next_pow2_at_least(int v, int lo) {
   return r;
 }
 
-}  // namespace
+struct DecodePlan {
+  int total_kb, npad, ks, stages;
+  uint32_t ssum_offset, slot_offset;
+  size_t smem;
+};
 
-cudaError_t setup_decode(const DeviceInfo&) {
-  for (const void* f : {reinterpret_cast<const void*>(decode_kernel<false>),
-                        reinterpret_cast<const void*>(decode_kernel<true>)}) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
-}
-
-cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
-  DecodeParams p{};
-  p.shared = a.shared;
-  p.out = a.out;
-  p.P = a.P;
-  p.T = a.T;
-  p.L = a.L;
-  p.H = a.H;
-  p.col_start = a.col_start;
-  p.col_end = a.col_end;
-  p.total_kb = ceil_div(a.L, kBlockK);
-  p.npad = ceil_div(std::max(a.T, 1), 16) * 16;
-  // K split: a fixed function of (T, L), never of the column range, so every
-  // output element is summed in the same order whatever range is requested.
-  // Four slices (224 CTAs at H = 7168, two per SM) when their buffers fit in
-  // half an SM's shared memory, else two (112 CTAs, one per SM), else one.
-  const uint32_t stage_bytes = kWStageBytes + static_cast<uint32_t>(p.npad) * 128u;
+// K split, stage count and shared-memory layout: a fixed function of (T, L),
+// never of the column range, so every output element is summed in the same
+// order whatever range is requested. Four slices (224 CTAs at H = 7168, two per
+// SM) when their buffers fit in half an SM's shared memory, else two (112 CTAs,
+// one per SM), else one. Returns false when even that does not fit.
+bool plan_decode(int T, int L, DecodePlan& g) {
+  if (T < 1 || T > kDecodeMaxTokens || L < 1) return false;
+  g.total_kb = ceil_div(L, kBlockK);
+  g.npad = ceil_div(T, 16) * 16;
+  const uint32_t stage_bytes = kWStageBytes + static_cast<uint32_t>(g.npad) * 128u;
   // The received K-slice partials take 128 rows x npad FP32 whatever the split.
   // Above 32 tokens they reuse the ring (one more cluster barrier, more stages:
   // the region is then the larger of the two), else they have their own bytes.
-  const bool in_ring = p.npad > 32;
-  const size_t sl = (static_cast<size_t>(kBlockM) * p.npad * 4 + 1023) & ~size_t(1023);
+  const bool in_ring = g.npad > 32;
+  const size_t sl = (static_cast<size_t>(kBlockM) * g.npad * 4 + 1023) & ~size_t(1023);
   auto ss_bytes = [&](int cand) {
-    return (static_cast<size_t>(p.npad) * (kBlockM / cand) * 4 + 1023) & ~size_t(1023);
+    return (static_cast<size_t>(g.npad) * (kBlockM / cand) * 4 + 1023) & ~size_t(1023);
   };
   auto region_for = [&](long st) {
     const size_t ring = static_cast<size_t>(st) * stage_bytes;
@@ -434,11 +421,11 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
   int ks = 1;
   int stages = 1;
   for (int cand : {4, 2}) {
-    if (p.total_kb < 4 * cand) continue;  // at least 4 K-blocks per slice
+    if (g.total_kb < 4 * cand) continue;  // at least 4 K-blocks per slice
     const long budget = cand == 4 ? kHalfSmBudget : kSmemBudget;
     long st = (budget - 1024 - static_cast<long>(ss_bytes(cand)) - fixed_extra) /
               static_cast<long>(stage_bytes);
-    st = std::min<long>({st, ceil_div(p.total_kb, cand), kMaxStages});
+    st = std::min<long>({st, ceil_div(g.total_kb, cand), kMaxStages});
     if (st < (cand == 4 ? 3 : 2) || smem_for(cand, st) > static_cast<size_t>(budget)) continue;
     ks = cand;
     stages = static_cast<int>(st);
@@ -447,14 +434,54 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
   if (ks == 1) {
     const long st = (kSmemBudget - 1024 - static_cast<long>(ss_bytes(1)) - fixed_extra) /
                     static_cast<long>(stage_bytes);
-    stages = static_cast<int>(std::max<long>(1, std::min<long>({st, p.total_kb, kMaxStages})));
+    stages = static_cast<int>(std::max<long>(1, std::min<long>({st, g.total_kb, kMaxStages})));
   }
   const size_t region = region_for(stages);
-  p.ks = ks;
-  p.kb_per_cta = ceil_div(p.total_kb, ks);
-  p.stages = stages;
-  p.ssum_offset = static_cast<uint32_t>(region);
-  p.slot_offset = in_ring ? 0u : static_cast<uint32_t>(region + ss_bytes(ks));
+  g.ks = ks;
+  g.stages = stages;
+  g.ssum_offset = static_cast<uint32_t>(region);
+  g.slot_offset = in_ring ? 0u : static_cast<uint32_t>(region + ss_bytes(ks));
+  g.smem = smem_for(ks, stages);
+  return g.smem <= static_cast<size_t>(kSmemLimit);
+}
+
+}  // namespace
+
+cudaError_t setup_decode(const DeviceInfo&) {
+  for (const void* f : {reinterpret_cast<const void*>(decode_kernel<false>),
+                        reinterpret_cast<const void*>(decode_kernel<true>)}) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+bool decode_supported(int T, int L) {
+  DecodePlan g;
+  return plan_decode(T, L, g);
+}
+
+cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+  DecodePlan g;
+  if (!plan_decode(a.T, a.L, g)) return cudaErrorInvalidConfiguration;
+  DecodeParams p{};
+  p.shared = a.shared;
+  p.out = a.out;
+  p.P = a.P;
+  p.T = a.T;
+  p.L = a.L;
+  p.H = a.H;
+  p.col_start = a.col_start;
+  p.col_end = a.col_end;
+  p.total_kb = g.total_kb;
+  p.npad = g.npad;
+  p.ks = g.ks;
+  p.kb_per_cta = ceil_div(g.total_kb, g.ks);
+  p.stages = g.stages;
+  p.ssum_offset = g.ssum_offset;
+  p.slot_offset = g.slot_offset;
+  const int ks = g.ks;
   p.tmem_cols = next_pow2_at_least(p.npad, 32);
   p.pdl = a.pdl ? 1 : 0;
   p.inputs_ready = a.inputs_ready ? 1 : 0;
@@ -464,8 +491,7 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
   const int tile_last = (a.col_end - 1) / kBlockM;
   p.tile0 = tile_first;
   const int ntiles = tile_last - tile_first + 1;
-  const size_t smem = smem_for(ks, stages);
-  if (smem > static_cast<size_t>(kSmemLimit)) return cudaErrorInvalidConfiguration;
+  const size_t smem = g.smem;
 
   CUtensorMap w_map, y_map;
   if (!make_map_bf16_sw128(&w_map, a.W, a.H, a.L, kBlockM)) return cudaErrorInvalidValue;

@@ -11,9 +11,12 @@ namespace lt {
 // Device error word bits (set with atomicOr by kernels, read by latent_tail_check).
 constexpr uint32_t kErrWaitTimeout = 1u;
 
-// Largest token count the decode (split-K, swap-AB) kernel serves; above it
-// the persistent tensor-core kernel runs.
-constexpr int kDecodeMaxTokens = 128;
+// Largest token count the decode (split-K, swap-AB) kernel serves; above it,
+// or when its buffers do not fit (decode_supported), the persistent
+// tensor-core kernel runs. Set where the two kernels cross over at L = 2048,
+// H = 7168, P = 8 (forward call, GB300): 21.4 against 23.7 us at T = 224,
+// 25.8 against 24.4 us at T = 256.
+constexpr int kDecodeMaxTokens = 224;
 
 // Up to this many tokens a call runs the CUDA-core kernel that does the whole
 // tail in one launch (gemv.cu), when one SM's slice of W fits in its shared
@@ -103,6 +106,9 @@ cudaError_t launch_stage(const void* src, void* dst, size_t bytes, const DeviceI
                          cudaStream_t stream);
 // Whether launch_gemv serves this shape on this device (T and the W slice fit).
 bool gemv_supported(int T, int L, int col_start, int col_end, const DeviceInfo& dev);
+// Whether launch_decode serves T tokens of latent width L (T <= kDecodeMaxTokens
+// and its buffers fit in shared memory; always true for T <= 128).
+bool decode_supported(int T, int L);
 cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 

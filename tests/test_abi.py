@@ -163,11 +163,15 @@ def test_host_workspace_size(lib):
     # decode sizes: the latent only (the kernels reach the host buffers directly)
     assert hws(8, 16, 2048, 7168) == lib.latent_tail_workspace_size(8, 16, 2048, 7168)
     assert hws(8, 128, 2048, 7168) == 128 * 2048 * 2
-    # above 128 tokens: latent + staging for routed, shared and out, each 256-rounded
-    P, T, L, H = 2, 129, 64, 128
+    assert hws(8, 224, 2048, 7168) == 224 * 2048 * 2  # the decode kernel's largest call
+    # the persistent kernel (above 224 tokens, or 224 tokens at a latent too
+    # narrow for the decode kernel's buffers): latent + staging for routed,
+    # shared and out, each 256-rounded
     r256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
-    assert hws(P, T, L, H) == r256(T * L * 2) + r256(P * T * L * 2) + r256(P * T * H * 2) \
-        + r256(T * H * 2)
+    for P, T, L, H in [(2, 225, 64, 128), (2, 224, 64, 128)]:
+        assert hws(P, T, L, H) == r256(T * L * 2) + r256(P * T * L * 2) + \
+            r256(P * T * H * 2) + r256(T * H * 2)
+    assert hws(2, 129, 64, 128) == 129 * 64 * 2 + 128  # decode kernel: latent only
     assert hws(8, 0, 2048, 7168) == 0
     assert hws(8, 16, 2047, 7168) == 0
 
@@ -188,7 +192,7 @@ def fwd_host(lib, routed=A, shared=B, g=C, W=D, out=E, P=2, T=4, L=64, H=128, ep
     (dict(routed=A + 8), Status.ALIGNMENT),
     (dict(ws=None), Status.WORKSPACE),
     (dict(wsb=100), Status.WORKSPACE),
-    (dict(T=200, wsb=200 * 64 * 2 + 256), Status.WORKSPACE),  # staging not included
+    (dict(T=300, wsb=300 * 64 * 2 + 256), Status.WORKSPACE),  # staging not included
     (dict(ws=WS + 8), Status.ALIGNMENT),
     (dict(g=C + 4), Status.ALIGNMENT),
     (dict(out=A + 64), Status.INVALID_ARG),   # out overlaps routed

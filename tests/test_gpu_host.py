@@ -31,19 +31,20 @@ def _host_result(x, g, ws=None, out_host=None, hr=None, hs=None):
 
 @pytest.mark.parametrize("P,T,L,H", [(8, 16, 2048, 7168), (8, 1, 2048, 7168), (8, 4, 2048, 7168),
                                      (3, 2, 512, 1032), (3, 5, 512, 1032),
-                                     (8, 128, 2048, 7168), (2, 200, 1024, 1024)])
+                                     (8, 128, 2048, 7168), (2, 200, 1024, 1024),
+                                     (2, 300, 1024, 1024)])
 def test_host_matches_device_bitwise(P, T, L, H):
     x = inputs.make(P, T, L, H, seed=7000 + T, device="cuda")
     assert torch.equal(_host_result(x, x.g), _device_result(x, x.g))
 
 
-@pytest.mark.parametrize("T", [2, 16, 200])
+@pytest.mark.parametrize("T", [2, 16, 200, 300])
 def test_host_no_norm(T):
     x = inputs.make(4, T, 1024, 2048, seed=7100 + T, device="cuda")
     assert torch.equal(_host_result(x, None), _device_result(x, None))
 
 
-@pytest.mark.parametrize("T", [2, 16, 200])
+@pytest.mark.parametrize("T", [2, 16, 200, 300])
 def test_host_in_place_into_shared_partial(T):
     P, L, H = 4, 1024, 2048
     x = inputs.make(P, T, L, H, seed=7200 + T, device="cuda")

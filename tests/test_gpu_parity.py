@@ -45,15 +45,17 @@ def test_decode_sweep(w):
     (1, 1, 64, 128),       # single token, single partial, one tile
     (3, 7, 328, 1000),     # ragged K-block (328 = 5*64 + 8) and ragged 128-row tile
     (5, 17, 2048, 520),    # tokens not a multiple of 16
-    (2, 128, 512, 384),    # largest decode token count
-    (3, 129, 328, 1000),   # smallest prefill token count, ragged everywhere
+    (2, 128, 512, 384),    # decode, 128 tokens
+    (2, 224, 512, 384),    # largest decode token count (two K slices)
+    (3, 129, 328, 1000),   # decode above 128 tokens with one K slice, ragged everywhere
+    (3, 225, 328, 1000),   # smallest prefill token count, ragged everywhere
     (2, 300, 192, 776),    # several 128-token tiles plus a tail; ragged 256-col tile
     (4, 520, 2048, 512),   # several token tiles at the production latent width
     (1, 1000, 64, 2056),   # many tiles, one K-block, P = 1 (pre-reduced latent)
     (16, 200, 256, 264),   # P = 16 partials
     (64, 4, 256, 256),     # P = 64, the largest partial count accepted (decode)
     (64, 2, 256, 256),     # P = 64 on the one-launch kernel
-    (64, 200, 128, 256),   # P = 64 on the prefill path
+    (64, 240, 128, 256),   # P = 64 on the prefill path
     (2, 8, 16384, 256),    # L = 16384, the largest latent width accepted (decode)
     (2, 2, 4096, 256),     # T = 2 at L = 4096: the widest latent the one-launch kernel takes
     (2, 2, 8192, 256),     # T = 2 at L = 8192: too wide for it, the two-kernel path runs
@@ -64,7 +66,8 @@ def test_decode_sweep(w):
     (9, 2, 4096, 1024),    # one-launch: the widest latent (two pieces per thread), P = 9 (two batches)
     (2, 260, 16384, 128),  # L = 16384 on the prefill path
     (1, 3, 8, 8),          # L = H = 8, the smallest accepted: boxes wider than the tensor
-    (2, 130, 8, 16),       # the same on the prefill path
+    (2, 130, 8, 16),       # the same above 128 tokens (decode kernel)
+    (2, 230, 8, 16),       # the same on the prefill path
 ])
 def test_ragged_shapes(P, T, L, H):
     x = inputs.make(P, T, L, H, seed=P * 1000 + T)
