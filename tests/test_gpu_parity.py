@@ -88,6 +88,27 @@ def test_full_size_every_element(w):
         assert len(x.scaled_up) == len(x.scaled_down) == w.T // 100
 
 
+@pytest.mark.parametrize("T", [129, 160, 224, 225])
+def test_decode_tier_above_128_tokens(T):
+    """The decode kernel's range above 128 tokens at the production widths (P = 8,
+    L = 2048, H = 7168: two K slices, one CTA per SM, the K-slice partials in the
+    stage ring), every element; T = 225 is the first token count of the prefill
+    kernel."""
+    check_full(inputs.make(8, T, 2048, 7168, seed=1300 + T), what=f"T{T}")
+
+
+@pytest.mark.parametrize("T", [160, 224])
+def test_decode_tier_column_ranges_tile_the_full_call(T):
+    """Column ranges of the decode kernel above 128 tokens (tiles cut by the
+    range, partial first and last tiles) reproduce the full call bit for bit."""
+    x = gh.to_dev(inputs.make(8, T, 2048, 7168, seed=1400 + T))
+    full = gh.run(x)
+    pieces = torch.full_like(full, float("nan"))
+    for c0, c1 in ((0, 1000), (1000, 4104), (4104, 7160), (7160, 7168)):
+        gh.run(x, c0, c1, out=pieces)
+    assert torch.equal(pieces.view(torch.int16), full.view(torch.int16))
+
+
 @pytest.mark.parametrize("T", [1, 2, 3])
 def test_one_launch_token_counts(T):
     """T <= 2 at the production widths (P = 8, L = 2048, H = 7168): the CUDA-core
