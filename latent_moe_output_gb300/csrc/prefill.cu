@@ -1,4 +1,5 @@
-// Steps 3-5 of the latent-MoE tail for prefill-sized token counts (T > 128):
+// Steps 3-5 of the latent-MoE tail for prefill-sized token counts (T > 224, and
+// T > 128 when the decode kernel's buffers do not fit):
 //   out[t,h] = bf16_rn( sum_l y[t,l] * W[h,l] + sum_p shared[p,t,h] ),  h in [c0,c1)
 // The narrowed beta-add GEMM of PR #50383's `_shard_up_proj_tail`
 // (`hidden_shard.addmm_(latent, up_proj_shard.t())`), with the shared-partial
