@@ -13,11 +13,11 @@
 // then write y = (x * r) * g rounded to bf16. Memory-bound: P*L*2 bytes in,
 // L*2 bytes out per token, every load a 16-byte vector.
 //
-// Decode-sized calls (T <= 128) also pass the W rows the projection kernel is
-// about to stream: the grid then has at least one CTA per SM, and every CTA
-// issues bulk L2 prefetches of its share of those rows before the dependency
-// wait, so the HBM reads of W start while the preceding work is still
-// finishing. CTAs beyond the T token rows only prefetch (and wait, so the
+// Calls that the decode kernel serves also pass the W rows the projection
+// kernel is about to stream: the grid then has at least one CTA per SM, and
+// every CTA issues bulk L2 prefetches of its share of those rows before the
+// dependency wait, so the HBM reads of W start while the preceding work is
+// still finishing. CTAs beyond the T token rows only prefetch (and wait, so the
 // grid's completion still implies the preceding work's).
 #include "launch.h"
 #include "ptx.cuh"
