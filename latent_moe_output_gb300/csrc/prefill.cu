@@ -15,8 +15,9 @@
 // matter. Pairs of CTAs (a 2-CTA cluster) therefore share one tensor-core
 // product (tcgen05 cta_group::2, M = 256 tokens, N = tile width): each CTA loads
 // its own 128 tokens of y and half of the W tile, which halves the operand bytes
-// per CTA. The tile width is 256 columns, or 128 for T <= 256 so that the few
-// tiles of a short call still occupy twice the CTA pairs (a template parameter,
+// per CTA. The tile width is 256 columns; 128 for T <= 256 so that the few
+// tiles of a short call still occupy twice the CTA pairs, and 192 for
+// 256 < T <= 1024, where it fills the pairs' waves (a template parameter,
 // chosen from T alone).
 //
 // Persistent, warp-specialized kernel, one CTA per SM, 7 warps per CTA:
@@ -49,8 +50,16 @@ namespace lt {
 namespace {
 
 constexpr int kTileT = 128;   // tokens per CTA (half of the pair's MMA M = 256)
-constexpr int kTileH = 256;   // output columns per tile (MMA N), T > 256
+constexpr int kTileH = 256;   // output columns per tile (MMA N), T > 1024
 constexpr int kNarrowTileH = 128;  // T <= 256: twice the tiles, so twice the pairs busy
+// 256 < T <= 1024: 192-column tiles. At H = 7168 a 256-token group has 38 of
+// them, so two groups fill the 76 CTA pairs of a GB300 exactly (against 56 of
+// 76 with 256 columns), and four groups run in two full waves (against 84 or
+// 112 tiles for 76 pairs); each CTA takes in 15% fewer bytes per tile (y is the
+// same, W and the shared partials shrink), and at large T that costs more
+// than it saves.
+constexpr int kMidTileH = 192;
+constexpr int kMidTileMaxTokens = 1024;
 constexpr int kBlockK = 64;
 constexpr int kMaxStages = 6;
 constexpr int kChunk = 64;    // output columns per shared-partial box
@@ -83,6 +92,12 @@ constexpr int kSinglePartialSlots = 2;
 // 128-column tiles (T <= 256): 24 KB stages, six of them beside five slots.
 constexpr int kNarrowStages = 6;
 constexpr int kNarrowSlots = 5;
+// 192-column tiles: 28 KB stages; the split of the 256-column tiles with the
+// room left over given to one more slot (P <= 8), or 3 + 8 (P > 8).
+constexpr int kMidStagesFewPartials = 4;
+constexpr int kMidSlotsFewPartials = 7;
+constexpr int kMidStagesManyPartials = 3;
+constexpr int kMidSlotsManyPartials = 8;
 
 size_t smem_bytes(int stages, int slots, int tile_h) {
   return 1024 + static_cast<size_t>(stages) * stage_bytes_for(tile_h) +
@@ -93,7 +108,7 @@ struct PrefillParams {
   uint16_t* out;
   int P, T, L, H;
   int col_start, col_end;
-  int tile_h;       // output columns per tile: kTileH or kNarrowTileH
+  int tile_h;       // output columns per tile: kTileH, kMidTileH or kNarrowTileH
   int htile0;       // absolute index of the first tile_h-column tile
   int n_htiles;
   int n_tpairs;     // 256-token groups (one per CTA pair and tile)
@@ -477,13 +492,14 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 }  // namespace
 
 cudaError_t setup_prefill(const DeviceInfo&) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kTileH>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemLimit));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(prefill_kernel<kNarrowTileH>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmemLimit));
+  for (const void* f : {reinterpret_cast<const void*>(prefill_kernel<kTileH>),
+                        reinterpret_cast<const void*>(prefill_kernel<kMidTileH>),
+                        reinterpret_cast<const void*>(prefill_kernel<kNarrowTileH>)}) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(kSmemLimit));
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
@@ -497,7 +513,7 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   p.col_end = a.col_end;
   // A fixed function of T (never of the column range), so that every output
   // element is computed the same way whatever range a call asks for.
-  p.tile_h = a.T <= 2 * kTileT ? kNarrowTileH : kTileH;
+  p.tile_h = a.T <= 2 * kTileT ? kNarrowTileH : a.T <= kMidTileMaxTokens ? kMidTileH : kTileH;
   p.htile0 = a.col_start / p.tile_h;
   p.n_htiles = (a.col_end - 1) / p.tile_h - p.htile0 + 1;
   p.n_tpairs = ceil_div(a.T, 2 * kTileT);
@@ -508,6 +524,9 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   } else if (p.tile_h == kNarrowTileH) {
     p.stages = kNarrowStages;
     p.slots = kNarrowSlots;
+  } else if (p.tile_h == kMidTileH) {
+    p.stages = a.P <= 8 ? kMidStagesFewPartials : kMidStagesManyPartials;
+    p.slots = a.P <= 8 ? kMidSlotsFewPartials : kMidSlotsManyPartials;
   } else if (a.P <= 8) {
     p.stages = kStagesFewPartials;
     p.slots = kSlotsFewPartials;
@@ -562,6 +581,8 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   cfg.numAttrs = static_cast<unsigned>(n);
   if (p.tile_h == kNarrowTileH)
     return cudaLaunchKernelEx(&cfg, prefill_kernel<kNarrowTileH>, y_map, w_map, s_map, p);
+  if (p.tile_h == kMidTileH)
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<kMidTileH>, y_map, w_map, s_map, p);
   return cudaLaunchKernelEx(&cfg, prefill_kernel<kTileH>, y_map, w_map, s_map, p);
 }
 

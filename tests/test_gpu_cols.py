@@ -80,10 +80,11 @@ def test_stress_sixteen_shards_full_size():
 
 
 def test_single_tile_and_multi_tile_epilogues_agree_bitwise():
-    """T = 600, H = 7168: the full call has 84 tiles for 76 CTA pairs (two tiles for
-    some pairs: accumulators double-buffered), each 1792-column shard has 21 tiles (one
-    per pair: the shared sums are parked in the idle accumulator's TMEM columns while
-    the mainloop runs). Both must give the same bits."""
+    """T = 600, H = 7168 (192-column tiles): the full call has 114 tiles for 76 CTA
+    pairs (two tiles for some pairs: accumulators double-buffered), each 1792-column
+    shard has 30 (one per pair: the shared sums are parked in the idle accumulator's
+    TMEM columns while the mainloop runs; shards cut tiles, which start at absolute
+    multiples of 192). Both must give the same bits."""
     P, T, L, H = 8, 600, 2048, 7168
     x = gh.to_dev(inputs.make(P, T, L, H, seed=6007))
     full = gh.run(x)
