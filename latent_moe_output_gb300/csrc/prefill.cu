@@ -92,10 +92,11 @@ constexpr int kSinglePartialSlots = 2;
 // 128-column tiles (T <= 256): 24 KB stages, six of them beside five slots.
 constexpr int kNarrowStages = 6;
 constexpr int kNarrowSlots = 5;
-// 192-column tiles: 28 KB stages; the split of the 256-column tiles with the
-// room left over given to one more slot (P <= 8), or 3 + 8 (P > 8).
-constexpr int kMidStagesFewPartials = 4;
-constexpr int kMidSlotsFewPartials = 7;
+// 192-column tiles: 28 KB stages. P = 8 (forward call, us, same box; 4 + 7,
+// 5 + 5, 3 + 8, 4 + 6): T = 320 26.40, 25.90, 28.87, 26.33; T = 640 47.23,
+// 45.38, 50.62, 46.78; T = 1024 51.50, 49.98, 55.09, 51.05. P > 8: 3 + 8.
+constexpr int kMidStagesFewPartials = 5;
+constexpr int kMidSlotsFewPartials = 5;
 constexpr int kMidStagesManyPartials = 3;
 constexpr int kMidSlotsManyPartials = 8;
 
