@@ -50,16 +50,15 @@ namespace lt {
 namespace {
 
 constexpr int kTileT = 128;   // tokens per CTA (half of the pair's MMA M = 256)
-constexpr int kTileH = 256;   // output columns per tile (MMA N), T > 1024
+constexpr int kTileH = 256;   // output columns per tile (MMA N)
 constexpr int kNarrowTileH = 128;  // T <= 256: twice the tiles, so twice the pairs busy
-// 256 < T <= 1024: 192-column tiles. At H = 7168 a 256-token group has 38 of
-// them, so two groups fill the 76 CTA pairs of a GB300 exactly (against 56 of
-// 76 with 256 columns), and four groups run in two full waves (against 84 or
-// 112 tiles for 76 pairs); each CTA takes in 15% fewer bytes per tile (y is the
-// same, W and the shared partials shrink), and at large T that costs more
-// than it saves.
+// 192-column tiles: at H = 7168 a 256-token group has 38 of them, so two
+// groups fill the 76 CTA pairs of a GB300 exactly (against 56 of 76 with 256
+// columns), and four groups run in two full waves (against 112 tiles for 76
+// pairs). A 192-column tile took ~0.9 of the time of a 256-column one in full
+// waves (P = 8), so the launch takes it when (waves with 192) x 9 <= (waves
+// with 256) x 10: at H = 7168, T in (256, 1024] and (1280, 1536].
 constexpr int kMidTileH = 192;
-constexpr int kMidTileMaxTokens = 1024;
 constexpr int kBlockK = 64;
 constexpr int kMaxStages = 6;
 constexpr int kChunk = 64;    // output columns per shared-partial box
@@ -514,7 +513,15 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   p.col_end = a.col_end;
   // A fixed function of T (never of the column range), so that every output
   // element is computed the same way whatever range a call asks for.
-  p.tile_h = a.T <= 2 * kTileT ? kNarrowTileH : a.T <= kMidTileMaxTokens ? kMidTileH : kTileH;
+  // (Of T, H and the device: a column range never changes it.)
+  if (a.T <= 2 * kTileT) {
+    p.tile_h = kNarrowTileH;
+  } else {
+    const int groups = ceil_div(a.T, 2 * kTileT);
+    const int pairs = std::max(1, dev.num_sms / 2);
+    auto waves = [&](int w) { return ceil_div(groups * ceil_div(a.H, w), pairs); };
+    p.tile_h = 9 * waves(kMidTileH) <= 10 * waves(kTileH) ? kMidTileH : kTileH;
+  }
   p.htile0 = a.col_start / p.tile_h;
   p.n_htiles = (a.col_end - 1) / p.tile_h - p.htile0 + 1;
   p.n_tpairs = ceil_div(a.T, 2 * kTileT);

@@ -46,7 +46,7 @@ def test_overlapping_output_is_rejected():
     (3, 2, 2048, 7168, 0, 7168), (3, 2, 2048, 7168, 1000, 5000),   # one-launch kernel
     (3, 16, 512, 1024, 0, 1024), (3, 16, 512, 1024, 256, 512),     # decode kernel
     (3, 300, 512, 1024, 0, 1024), (3, 300, 512, 1024, 128, 896),   # prefill, 192-col tiles
-    (3, 1100, 256, 1024, 0, 1024), (3, 1100, 256, 1024, 128, 896),  # prefill, 256-col tiles
+    (3, 3328, 256, 1024, 0, 1024), (3, 3328, 256, 1024, 128, 896),  # prefill, 256-col tiles
     (3, 200, 512, 1024, 0, 1024), (3, 200, 512, 1024, 128, 896),   # decode above 128 tokens
     (3, 240, 512, 1024, 0, 1024), (3, 240, 512, 1024, 128, 896),   # prefill, 128-col tiles
     (8, 1000, 2048, 7168, 0, 7168),                                # production widths

@@ -50,7 +50,7 @@ def test_decode_sweep(w):
     (3, 129, 328, 1000),   # decode above 128 tokens with one K slice, ragged everywhere
     (3, 225, 328, 1000),   # smallest prefill token count, ragged everywhere
     (2, 300, 192, 776),    # several 128-token tiles plus a tail; ragged 192-col tile
-    (2, 1100, 192, 776),   # the same with 256-col tiles (T > 1024)
+    (2, 4100, 192, 776),   # the same with 256-col tiles (17 token groups)
     (4, 520, 2048, 512),   # several token tiles at the production latent width
     (1, 1000, 64, 2056),   # many tiles, one K-block, P = 1 (pre-reduced latent)
     (16, 200, 256, 264),   # P = 16 partials
