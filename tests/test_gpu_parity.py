@@ -66,6 +66,9 @@ def test_decode_sweep(w):
     (7, 1, 2056, 7176),    # one-launch: 257 latent pieces (two for thread 0), P = 7, last CTA 24 rows
     (9, 2, 4096, 1024),    # one-launch: the widest latent (two pieces per thread), P = 9 (two batches)
     (2, 260, 16384, 128),  # L = 16384 on the prefill path
+    (2, 200, 16384, 136),  # L = 16384 on the decode kernel above 128 tokens (two K slices)
+    (64, 160, 256, 256),   # P = 64 on the decode kernel above 128 tokens (one K slice)
+    (1, 200, 64, 2056),    # P = 1, one K-block, 200 tokens on the decode kernel
     (1, 3, 8, 8),          # L = H = 8, the smallest accepted: boxes wider than the tensor
     (2, 130, 8, 16),       # the same above 128 tokens (decode kernel)
     (2, 230, 8, 16),       # the same on the prefill path
