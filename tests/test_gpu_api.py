@@ -109,7 +109,7 @@ def test_side_stream_and_repeat_determinism():
         assert torch.equal(gh.run(x), a)
 
 
-@pytest.mark.parametrize("T", [16, 64, 128, 256])
+@pytest.mark.parametrize("T", [16, 64, 128, 200, 256])
 def test_back_to_back_calls_read_what_the_previous_call_wrote(T):
     """Each call's output is every input of the next one (P = 1, T = H = L: the
     output [T, H] doubles as latent/routed [T, L], shared [1, T, H] and W [H, L]).

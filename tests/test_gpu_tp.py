@@ -25,7 +25,7 @@ def _free_port():
 
 
 @pytest.mark.parametrize("exchange", ["all_reduce", "all_gather"])
-@pytest.mark.parametrize("T", [16, 300])
+@pytest.mark.parametrize("T", [16, 200, 300])
 def test_one_rank_nccl_group_matches_oracle(exchange, T):
     gh.library()
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(_free_port()))
