@@ -95,6 +95,10 @@ def flops(T, L, width):
     return 2 * T * width * L
 
 
+# Largest token count the decode kernel serves at the bench's widths (L = 2048).
+DECODE_TOKENS = 224
+
+
 def profiled_traffic(kernel, workload_name, T):
     """DRAM bytes per launch of `kernel` (dram__bytes_read.sum + dram__bytes_write.sum)
     from the ncu summary committed under profiles/, or None when no capture matches
@@ -365,10 +369,10 @@ def roofline_of(w, us_proj, us_call, hbm, tc_burst, peak_kind):
     peak than its bytes at the HBM peak (the P = 1 prefill)."""
     P, T, L, H = w.P, w.T, w.L, w.H
     pb, cb, fl = project_bytes(P, T, L, H), call_bytes(P, T, L, H), flops(T, L, H)
-    # T <= 2 at these widths (one SM's W slice fits in shared memory): the
-    # one-launch CUDA-core kernel; up to 128 tokens the split-K decode kernel.
-    # which kernel a call runs at the bench's latent width (L = 2048)
-    kname = "gemv_kernel" if T <= 2 else "decode_kernel" if T <= 224 else "prefill_kernel"
+    # Which kernel a call runs at the bench's widths (L = 2048, H = 7168): T <= 2
+    # the one-launch CUDA-core kernel (one SM's W slice fits in shared memory),
+    # up to 224 tokens the split-K decode kernel, above it the prefill kernel.
+    kname = "gemv_kernel" if T <= 2 else "decode_kernel" if T <= DECODE_TOKENS else "prefill_kernel"
     proj_gbs = pb / (us_proj * 1e-6) / 1e9
     if fl / (tc_burst * 1e12) > pb / (hbm * 1e9):
         proj_tf = fl / (us_proj * 1e-6) / 1e12
@@ -533,7 +537,7 @@ def measure_extra(w, args, dev, rank, world, peak):
     rec = {"workload": w.name, "P": w.P, "T": w.T, "L": w.L, "H": w.H,
            "us_per_call": round(us_call, 3),
            "tokens_per_s": round(job_throughput(w.T, steps, world, t_call), 1),
-           "single_call_us_median": round(b.single_call_us(100 if w.T <= 128 else 5), 3),
+           "single_call_us_median": round(b.single_call_us(100 if w.T <= DECODE_TOKENS else 5), 3),
            "roofline": roof, "call_roofline": call_roof,
            "timing": f"median of {repeats} regions of {steps} graph-replayed calls"}
     b.release()
@@ -610,7 +614,7 @@ def ours(args):
                       "norm_once_us_per_step": round(t_once / shard_steps * 1e6, 3),
                       "norm_once_note": "latent_tail_norm once, then N latent_tail_project_cols"}
 
-    us_single = b.single_call_us(100 if T <= 128 else 5)
+    us_single = b.single_call_us(100 if T <= DECODE_TOKENS else 5)
 
     # End to end through the host-buffer entry point: every step takes its
     # partials from page-locked host memory and leaves its result there. The
@@ -698,7 +702,7 @@ def ours(args):
                 "us_per_step": round(t_e2e / e2e_steps * 1e6, 3),
                 "api": "latent_tail_forward_host (page-locked host partials and result; "
                        + ("kernels read/write them across the host link"
-                          if T <= 128 else "staged with one copy per tensor") + ")",
+                          if T <= DECODE_TOKENS else "staged with one copy per tensor") + ")",
                 "staged_copies_us_per_step": round(t_staged / e2e_steps * 1e6, 3),
                 "timing": f"median of {e2e_reps} regions, CUDA graphs, CUDA events, "
                           f"{n_host} pinned host set(s)"},
