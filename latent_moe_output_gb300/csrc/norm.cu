@@ -9,7 +9,8 @@
 //
 // One CTA per token row: 256 threads each own 8-element (16-byte) chunks of
 // the row, load all P partials of a chunk before accumulating (p ascending),
-// keep x in shared memory, reduce the sum of squares with warp shuffles and
+// keep x in registers (L <= 2048: one chunk per thread) or else in shared
+// memory, reduce the sum of squares with warp shuffles and
 // then write y = (x * r) * g rounded to bf16. Memory-bound: P*L*2 bytes in,
 // L*2 bytes out per token, every load a 16-byte vector.
 //
@@ -49,11 +50,15 @@ __device__ __forceinline__ void add8(float (&a)[8], const uint4& v) {
   a[7] += bf16_hi(v.w);
 }
 
+// kRegs: L <= 8 * kNormThreads, so each thread owns at most one 8-element chunk
+// and keeps it in registers between the reduction and the write (no shared
+// memory for x, fewer registers than staging it through shared memory).
+template <bool kRegs>
 __global__ void __launch_bounds__(kNormThreads)
     norm_kernel(const uint16_t* __restrict__ routed, const float* __restrict__ g,
                 uint16_t* __restrict__ y, int P, int T, int L, float eps, int trigger,
                 const uint8_t* __restrict__ pf, size_t pf_bytes, size_t pf_routed_bytes) {
-  extern __shared__ float4 xs4[];  // the token's x[L] in FP32
+  extern __shared__ float4 xs4[];  // !kRegs: the token's x[L] in FP32
   __shared__ float red[kNormThreads / 32];
   // Optional: pull `routed` and then the projection's W rows into L2 before
   // waiting, spread over the CTAs of the grid first (piece i goes to CTA
@@ -93,6 +98,9 @@ __global__ void __launch_bounds__(kNormThreads)
   const uint16_t* base = routed + static_cast<size_t>(t) * L;
 
   float ss = 0.f;
+  float keep[8];  // kRegs: this thread's chunk of x
+#pragma unroll
+  for (int j = 0; j < 8; ++j) keep[j] = 0.f;
   for (int c = threadIdx.x; c < nchunk; c += kNormThreads) {
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const uint16_t* src = base + static_cast<size_t>(c) * 8;
@@ -107,8 +115,13 @@ __global__ void __launch_bounds__(kNormThreads)
     for (; p < P; ++p) add8(a, ld_stream_v4(src + p * row_stride));
 #pragma unroll
     for (int j = 0; j < 8; ++j) ss += a[j] * a[j];
-    xs4[2 * c] = make_float4(a[0], a[1], a[2], a[3]);
-    xs4[2 * c + 1] = make_float4(a[4], a[5], a[6], a[7]);
+    if constexpr (kRegs) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) keep[j] = a[j];
+    } else {
+      xs4[2 * c] = make_float4(a[0], a[1], a[2], a[3]);
+      xs4[2 * c + 1] = make_float4(a[4], a[5], a[6], a[7]);
+    }
   }
 
   ss = warp_sum(ss);
@@ -124,27 +137,29 @@ __global__ void __launch_bounds__(kNormThreads)
   const float r = 1.0f / sqrtf(red[0] / static_cast<float>(L) + eps);
 
   uint4* dst = reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * L);
-  if (g == nullptr) {  // no norm: round the partial sum itself
-    for (int c = threadIdx.x; c < nchunk; c += kNormThreads) {
-      const float4 x0 = xs4[2 * c], x1 = xs4[2 * c + 1];
-      uint4 o;
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  for (int c = threadIdx.x; c < nchunk; c += kNormThreads) {
+    float4 x0, x1;
+    if constexpr (kRegs) {
+      x0 = make_float4(keep[0], keep[1], keep[2], keep[3]);
+      x1 = make_float4(keep[4], keep[5], keep[6], keep[7]);
+    } else {
+      x0 = xs4[2 * c];
+      x1 = xs4[2 * c + 1];
+    }
+    uint4 o;
+    if (g == nullptr) {  // no norm: round the partial sum itself
       o.x = pack_bf16x2(x0.x, x0.y);
       o.y = pack_bf16x2(x0.z, x0.w);
       o.z = pack_bf16x2(x1.x, x1.y);
       o.w = pack_bf16x2(x1.z, x1.w);
-      dst[c] = o;
+    } else {
+      const float4 g0 = __ldg(g4 + 2 * c), g1 = __ldg(g4 + 2 * c + 1);
+      o.x = pack_bf16x2(x0.x * r * g0.x, x0.y * r * g0.y);
+      o.y = pack_bf16x2(x0.z * r * g0.z, x0.w * r * g0.w);
+      o.z = pack_bf16x2(x1.x * r * g1.x, x1.y * r * g1.y);
+      o.w = pack_bf16x2(x1.z * r * g1.z, x1.w * r * g1.w);
     }
-    return;
-  }
-  const float4* g4 = reinterpret_cast<const float4*>(g);
-  for (int c = threadIdx.x; c < nchunk; c += kNormThreads) {
-    const float4 x0 = xs4[2 * c], x1 = xs4[2 * c + 1];
-    const float4 g0 = __ldg(g4 + 2 * c), g1 = __ldg(g4 + 2 * c + 1);
-    uint4 o;
-    o.x = pack_bf16x2(x0.x * r * g0.x, x0.y * r * g0.y);
-    o.y = pack_bf16x2(x0.z * r * g0.z, x0.w * r * g0.w);
-    o.z = pack_bf16x2(x1.x * r * g1.x, x1.y * r * g1.y);
-    o.w = pack_bf16x2(x1.z * r * g1.z, x1.w * r * g1.w);
     dst[c] = o;
   }
 }
@@ -152,7 +167,7 @@ __global__ void __launch_bounds__(kNormThreads)
 }  // namespace
 
 cudaError_t setup_norm(const DeviceInfo&) {
-  return cudaFuncSetAttribute(norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(norm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kMaxL * static_cast<int>(sizeof(float)));
 }
 
@@ -170,17 +185,20 @@ cudaError_t launch_norm(const NormArgs& a, bool trigger_dependents, const Device
       a.l2_prefetch_bytes != 0 || pf_routed != 0 ? std::max(a.T, dev.num_sms) : a.T;
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kNormThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(a.L) * sizeof(float);
+  const bool regs = a.L <= 8 * kNormThreads;  // one 8-element chunk per thread at most
+  cfg.dynamicSmemBytes = regs ? 0 : static_cast<size_t>(a.L) * sizeof(float);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, norm_kernel, a.routed, a.g, a.y, a.P, a.T, a.L, a.eps,
-                            trigger_dependents ? 1 : 0,
-                            static_cast<const uint8_t*>(a.l2_prefetch), a.l2_prefetch_bytes,
-                            pf_routed);
+  const int trig = trigger_dependents ? 1 : 0;
+  const uint8_t* pf = static_cast<const uint8_t*>(a.l2_prefetch);
+  return regs ? cudaLaunchKernelEx(&cfg, norm_kernel<true>, a.routed, a.g, a.y, a.P, a.T, a.L,
+                                   a.eps, trig, pf, a.l2_prefetch_bytes, pf_routed)
+              : cudaLaunchKernelEx(&cfg, norm_kernel<false>, a.routed, a.g, a.y, a.P, a.T, a.L,
+                                   a.eps, trig, pf, a.l2_prefetch_bytes, pf_routed);
 }
 
 }  // namespace lt
