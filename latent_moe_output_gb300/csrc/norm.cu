@@ -98,6 +98,15 @@ __global__ void __launch_bounds__(kNormThreads)
   const uint16_t* base = routed + static_cast<size_t>(t) * L;
 
   float ss = 0.f;
+  // kRegs: the weights of this thread's single chunk are requested now, with
+  // its partials, instead of after the reduction (one round trip less on the
+  // path to y).
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  float4 g0_reg = make_float4(0.f, 0.f, 0.f, 0.f), g1_reg = g0_reg;
+  if (kRegs && g != nullptr && static_cast<int>(threadIdx.x) < nchunk) {
+    g0_reg = __ldg(g4 + 2 * threadIdx.x);
+    g1_reg = __ldg(g4 + 2 * threadIdx.x + 1);
+  }
   float keep[8];  // kRegs: this thread's chunk of x
 #pragma unroll
   for (int j = 0; j < 8; ++j) keep[j] = 0.f;
@@ -128,16 +137,12 @@ __global__ void __launch_bounds__(kNormThreads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) red[warp] = ss;
   __syncthreads();
-  if (warp == 0) {
-    float v = lane < kNormThreads / 32 ? red[lane] : 0.f;
-    v = warp_sum(v);
-    if (lane == 0) red[0] = v;
-  }
-  __syncthreads();
-  const float r = 1.0f / sqrtf(red[0] / static_cast<float>(L) + eps);
+  // The eight warp sums, added in the order of a halving shuffle tree over them.
+  static_assert(kNormThreads == 256, "eight warp sums");
+  const float total = ((red[0] + red[4]) + (red[2] + red[6])) + ((red[1] + red[5]) + (red[3] + red[7]));
+  const float r = 1.0f / sqrtf(total / static_cast<float>(L) + eps);
 
   uint4* dst = reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * L);
-  const float4* g4 = reinterpret_cast<const float4*>(g);
   for (int c = threadIdx.x; c < nchunk; c += kNormThreads) {
     float4 x0, x1;
     if constexpr (kRegs) {
@@ -154,7 +159,8 @@ __global__ void __launch_bounds__(kNormThreads)
       o.z = pack_bf16x2(x1.x, x1.y);
       o.w = pack_bf16x2(x1.z, x1.w);
     } else {
-      const float4 g0 = __ldg(g4 + 2 * c), g1 = __ldg(g4 + 2 * c + 1);
+      const float4 g0 = kRegs ? g0_reg : __ldg(g4 + 2 * c);
+      const float4 g1 = kRegs ? g1_reg : __ldg(g4 + 2 * c + 1);
       o.x = pack_bf16x2(x0.x * r * g0.x, x0.y * r * g0.y);
       o.y = pack_bf16x2(x0.z * r * g0.z, x0.w * r * g0.w);
       o.z = pack_bf16x2(x1.x * r * g1.x, x1.y * r * g1.y);
