@@ -378,7 +378,8 @@ def roofline_of(w, us_proj, us_call, hbm, tc_burst, peak_kind):
         proj_tf = fl / (us_proj * 1e-6) / 1e12
         roof = {"kernel": kname, "bound": "tensor", "achieved": round(proj_tf, 1),
                 "peak": tc_burst, "unit": "TFLOP/s", "frac": round(proj_tf / tc_burst, 4),
-                "traffic": None, "algorithmic_flops_per_launch": fl,
+                "traffic": profiled_traffic(kname, w.name, T), "algorithmic_bytes_per_launch": pb,
+                "algorithmic_flops_per_launch": fl,
                 "us_per_launch": round(us_proj, 3), "peak_source": peak_kind}
     else:
         roof = {"kernel": kname, "bound": "hbm", "achieved": round(proj_gbs, 1), "peak": hbm,
