@@ -69,7 +69,38 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps")
     ap.add_argument("--shards", type=int, default=0,
                     help="also time each step as N column-range calls covering [0, H)")
+    ap.add_argument("--capture", default="",
+                    help="comma-separated workloads (name or name@T): run one forward call "
+                         "of each, in order, and nothing else (a launch list for ncu)")
     return ap.parse_args()
+
+
+def capture_calls(spec):
+    """One forward call per listed workload, inputs resident in HBM, synchronized
+    after each: under ncu each kernel of the list is captured once, in order."""
+    import dataclasses
+
+    import torch
+
+    from latent_moe_output_gb300 import binding, inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    binding.load_library()
+    for item in spec.split(","):
+        name, _, t = item.partition("@")
+        w = workload(name)
+        if t:
+            w = dataclasses.replace(w, name=f"{w.name}_T{int(t)}", T=int(t))
+        x = inputs.make_workload(w, device=dev)
+        out = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(max(binding.latent_tail_workspace_size(w.P, w.T, w.L, w.H), 256),
+                         dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream(dev)
+        binding.latent_tail_forward(x.routed, x.shared, x.g, x.W, out, x.eps, ws, stream)
+        binding.latent_tail_check(stream)
+        print(f"captured call: workload {w.name}, P {w.P}, T {w.T}, L {w.L}, H {w.H}", flush=True)
+        del x, out, ws
 
 
 def workload(name):
@@ -720,7 +751,9 @@ def ours(args):
 
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.capture:
+        capture_calls(args.capture)
+    elif args.impl == "reference":
         reference_arm(args)
     else:
         ours(args)

@@ -45,6 +45,11 @@ constexpr uint32_t kWStageBytes = kBlockM * kBlockK * 2;  // 16 KB
 constexpr int kSmemLimit = 220 * 1024;                   // + static smem <= opt-in max
 constexpr int kSmemBudget = 210 * 1024;                   // one CTA per SM
 constexpr int kHalfSmBudget = 110 * 1024;                 // two CTAs per SM
+// Four K slices (two CTAs per SM) only up to this many padded tokens: at 97-112
+// tokens two slices on one CTA per SM were faster (GB300, P = 8, L = 2048,
+// H = 7168, forward call 15.6-15.9 against 16.7-17.2 us at T = 104 and 112),
+// at 96 and below four (14.0 against 14.8 us at T = 96, 13.1 against 15.0 at 80).
+constexpr int kFourSliceMaxNpad = 96;
 
 struct DecodeParams {
   const uint16_t* shared;
@@ -419,8 +424,9 @@ struct DecodePlan {
 // K split, stage count and shared-memory layout: a fixed function of (T, L),
 // never of the column range, so every output element is summed in the same
 // order whatever range is requested. Four slices (224 CTAs at H = 7168, two per
-// SM) when their buffers fit in half an SM's shared memory, else two (112 CTAs,
-// one per SM), else one. Returns false when even that does not fit.
+// SM) for up to 96 tokens when their buffers fit in half an SM's shared memory,
+// else two (112 CTAs, one per SM), else one. Returns false when even that does
+// not fit.
 bool plan_decode(int T, int L, DecodePlan& g) {
   if (T < 1 || T > kDecodeMaxTokens || L < 1) return false;
   g.total_kb = ceil_div(L, kBlockK);
@@ -446,6 +452,7 @@ bool plan_decode(int T, int L, DecodePlan& g) {
   int stages = 1;
   for (int cand : {4, 2}) {
     if (g.total_kb < 4 * cand) continue;  // at least 4 K-blocks per slice
+    if (cand == 4 && g.npad > kFourSliceMaxNpad) continue;
     const long budget = cand == 4 ? kHalfSmBudget : kSmemBudget;
     long st = (budget - 1024 - static_cast<long>(ss_bytes(cand)) - fixed_extra) /
               static_cast<long>(stage_bytes);

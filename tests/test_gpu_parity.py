@@ -101,9 +101,27 @@ def test_decode_tier_above_128_tokens(T):
     check_full(inputs.make(8, T, 2048, 7168, seed=1300 + T), what=f"T{T}")
 
 
-@pytest.mark.parametrize("T", [160, 224])
+@pytest.mark.parametrize("T", [72, 96, 97, 112])
+def test_decode_tier_around_the_slice_switch(T):
+    """The decode kernel keeps four K slices (two CTAs per SM) up to 96 tokens and
+    two slices (one CTA per SM) above: both sides of the switch, every element at
+    the production widths."""
+    check_full(inputs.make(8, T, 2048, 7168, seed=1500 + T), what=f"T{T}")
+
+
+@pytest.mark.parametrize("P,T,L,H", [
+    (2, 65, 64, 264),      # one K-block, one slice; the last 128-row tile has 8 rows
+    (3, 100, 328, 392),    # ragged K-block, one slice, last tile 8 rows
+    (2, 97, 512, 136),     # two slices just above the switch, last tile 8 rows
+    (5, 224, 1024, 520),   # the largest decode token count, five tiles
+])
+def test_decode_tier_ragged(P, T, L, H):
+    check_full(inputs.make(P, T, L, H, seed=P * 1000 + T + 7), what=f"P{P} T{T} L{L} H{H}")
+
+
+@pytest.mark.parametrize("T", [104, 160, 224])
 def test_decode_tier_column_ranges_tile_the_full_call(T):
-    """Column ranges of the decode kernel above 128 tokens (tiles cut by the
+    """Column ranges of the decode kernel with two K slices (tiles cut by the
     range, partial first and last tiles) reproduce the full call bit for bit."""
     x = gh.to_dev(inputs.make(8, T, 2048, 7168, seed=1400 + T))
     full = gh.run(x)
