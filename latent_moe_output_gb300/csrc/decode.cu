@@ -10,9 +10,9 @@
 //     columns h), its N are the T tokens padded to a multiple of 16, K = L;
 //     the FP32 accumulator D[h][t] lives in TMEM;
 //   * one CTA per (128-row tile, K slice); the KS slices of a tile form one
-//     thread-block cluster. KS = 4 (two CTAs per SM) while its buffers fit in
-//     half an SM, else 2. Clusters of 8 cannot all be resident at once, which
-//     is why the split stops at 4;
+//     thread-block cluster. KS = 8 for up to 16 tokens (four CTAs per SM),
+//     KS = 4 (two CTAs per SM) up to 96 tokens while its buffers fit in half
+//     an SM, else 2;
 //   * W boxes (128 x 64, 128-byte swizzle) are requested before the rest of the
 //     set-up, and under programmatic dependent launch before waiting for the
 //     norm kernel that writes y (which has already prefetched W into L2); one
@@ -50,6 +50,17 @@ constexpr int kHalfSmBudget = 110 * 1024;                 // two CTAs per SM
 // H = 7168, forward call 15.6-15.9 against 16.7-17.2 us at T = 104 and 112),
 // at 96 and below four (14.0 against 14.8 us at T = 96, 13.1 against 15.0 at 80).
 constexpr int kFourSliceMaxNpad = 96;
+// Eight K slices (448 CTAs at H = 7168, clusters of 8, four CTAs per SM) for up to
+// 16 tokens: every SM then streams about the same share of W (against 256 KB on 72
+// SMs and 128 KB on the other 80 with four slices). Measured 1-3 % faster per call
+// at T = 3...16 (GB300, P = 8, L = 2048, H = 7168: T = 16 10.46-10.48 against
+// 10.58-10.63 us, T = 3 9.58 against 9.83-9.88 us).
+constexpr int kEightSliceMaxNpad = 16;
+constexpr int kQuarterSmBudget = 55 * 1024;  // four CTAs per SM
+
+constexpr int kTwoPerSm = 0;
+constexpr int kOnePerSmMode = 1;
+constexpr int kFourPerSm = 2;
 
 struct DecodeParams {
   const uint16_t* shared;
@@ -96,11 +107,14 @@ __device__ __forceinline__ void add8(float (&a)[8], const uint4& v) {
 //                      src; above 32 tokens slot_offset is 0: the partials then reuse
 //                      the ring once every CTA of the cluster has finished its MMAs,
 //                      which leaves room for more stages (region = the larger of the two)
-// kOnePerSm: the launch has one CTA per SM (KS <= 2); see (a) below.
-template <bool kOnePerSm>
-__global__ void __launch_bounds__(kThreads, 1)
+// kMode: how many CTAs the launch puts on an SM. kTwoPerSm (KS = 4), kOnePerSm
+// (KS <= 2; see (a) below) or kFourPerSm (KS = 8, register use capped so that
+// four CTAs fit in the register file).
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, kMode == kFourPerSm ? 4 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap w_map,
                   const __grid_constant__ CUtensorMap y_map, const DecodeParams p) {
+  constexpr bool kOnePerSm = kMode == kOnePerSmMode;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[kMaxStages];
   __shared__ uint64_t empty_bar[kMaxStages];
@@ -423,10 +437,11 @@ struct DecodePlan {
 
 // K split, stage count and shared-memory layout: a fixed function of (T, L),
 // never of the column range, so every output element is summed in the same
-// order whatever range is requested. Four slices (224 CTAs at H = 7168, two per
-// SM) for up to 96 tokens when their buffers fit in half an SM's shared memory,
-// else two (112 CTAs, one per SM), else one. Returns false when even that does
-// not fit.
+// order whatever range is requested. Eight slices (448 CTAs at H = 7168, four
+// per SM) for up to 16 tokens when their buffers fit in a quarter of an SM's
+// shared memory, four (224 CTAs, two per SM) for up to 96 tokens when they fit
+// in half, else two (112 CTAs, one per SM), else one. Returns false when even
+// that does not fit.
 bool plan_decode(int T, int L, DecodePlan& g) {
   if (T < 1 || T > kDecodeMaxTokens || L < 1) return false;
   g.total_kb = ceil_div(L, kBlockK);
@@ -450,10 +465,13 @@ bool plan_decode(int T, int L, DecodePlan& g) {
   const long fixed_extra = in_ring ? 0 : static_cast<long>(sl);
   int ks = 1;
   int stages = 1;
-  for (int cand : {4, 2}) {
+  for (int cand : {8, 4, 2}) {
     if (g.total_kb < 4 * cand) continue;  // at least 4 K-blocks per slice
+    if ((cand - 1) * ceil_div(g.total_kb, cand) >= g.total_kb) continue;  // no empty slice
+    if (cand == 8 && g.npad > kEightSliceMaxNpad) continue;
     if (cand == 4 && g.npad > kFourSliceMaxNpad) continue;
-    const long budget = cand == 4 ? kHalfSmBudget : kSmemBudget;
+    const long budget =
+        cand == 8 ? kQuarterSmBudget : cand == 4 ? kHalfSmBudget : kSmemBudget;
     long st = (budget - 1024 - static_cast<long>(ss_bytes(cand)) - fixed_extra) /
               static_cast<long>(stage_bytes);
     st = std::min<long>({st, ceil_div(g.total_kb, cand), kMaxStages});
@@ -479,8 +497,9 @@ bool plan_decode(int T, int L, DecodePlan& g) {
 }  // namespace
 
 cudaError_t setup_decode(const DeviceInfo&) {
-  for (const void* f : {reinterpret_cast<const void*>(decode_kernel<false>),
-                        reinterpret_cast<const void*>(decode_kernel<true>)}) {
+  for (const void* f : {reinterpret_cast<const void*>(decode_kernel<kTwoPerSm>),
+                        reinterpret_cast<const void*>(decode_kernel<kOnePerSmMode>),
+                        reinterpret_cast<const void*>(decode_kernel<kFourPerSm>)}) {
     const cudaError_t e =
         cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return e;
@@ -548,8 +567,9 @@ cudaError_t launch_decode(const ProjectArgs& a, const DeviceInfo& dev, cudaStrea
   }
   cfg.attrs = attrs;
   cfg.numAttrs = static_cast<unsigned>(n);
-  return ks <= 2 ? cudaLaunchKernelEx(&cfg, decode_kernel<true>, w_map, y_map, p)
-                 : cudaLaunchKernelEx(&cfg, decode_kernel<false>, w_map, y_map, p);
+  if (ks == 8) return cudaLaunchKernelEx(&cfg, decode_kernel<kFourPerSm>, w_map, y_map, p);
+  return ks <= 2 ? cudaLaunchKernelEx(&cfg, decode_kernel<kOnePerSmMode>, w_map, y_map, p)
+                 : cudaLaunchKernelEx(&cfg, decode_kernel<kTwoPerSm>, w_map, y_map, p);
 }
 
 }  // namespace lt

@@ -45,6 +45,7 @@ def test_decode_sweep(w):
     (1, 1, 64, 128),       # single token, single partial, one tile
     (3, 7, 328, 1000),     # ragged K-block (328 = 5*64 + 8) and ragged 128-row tile
     (5, 17, 2048, 520),    # tokens not a multiple of 16
+    (3, 13, 2248, 392),    # eight K slices (T <= 16), the last one a single ragged K-block
     (2, 128, 512, 384),    # decode, 128 tokens
     (2, 224, 512, 384),    # largest decode token count (two K slices)
     (3, 129, 328, 1000),   # decode above 128 tokens with one K slice, ragged everywhere
