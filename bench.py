@@ -33,7 +33,9 @@ the device entry point.
 
 Prints one JSON line. `--impl reference` times the CPU oracle instead (the
 only other code path this file may run), on a bounded sample of the same
-workload.
+workload. `--capture w1,w2@T,...` prints no JSON: it runs one forward call per
+listed workload and nothing else, the launch list that one ncu pass captures
+for the per-workload DRAM traffic figures.
 """
 
 from __future__ import annotations
