@@ -117,3 +117,17 @@ def test_reference_arm_prints_one_complete_line(capsys, monkeypatch):
     monkeypatch.setenv("RANK", "1")
     bench.reference_arm(args)
     assert capsys.readouterr().out.strip() == ""
+
+
+def test_every_benchmark_workload_has_current_traffic():
+    """Every configuration bench.py reports (the headline and its workloads record)
+    has a DRAM-traffic figure under profiles/ taken on the current source of the
+    kernel that dominates it: a kernel change without a new capture fails here."""
+    from latent_moe_output_gb300 import inputs
+
+    names = ["stress", "prefill", "prefill_p1", "decode"] + [w.name for w in inputs.DECODE_SWEEP]
+    for name in names:
+        w = inputs.WORKLOADS[name]
+        kname = ("gemv_kernel" if w.T <= 2 else
+                 "decode_kernel" if w.T <= bench.DECODE_TOKENS else "prefill_kernel")
+        assert bench.profiled_traffic(kname, w.name, w.T) is not None, (name, kname)
