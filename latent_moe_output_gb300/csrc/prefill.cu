@@ -16,9 +16,11 @@
 // product (tcgen05 cta_group::2, M = 256 tokens, N = tile width): each CTA loads
 // its own 128 tokens of y and half of the W tile, which halves the operand bytes
 // per CTA. The tile width is 256 columns; 128 for T <= 256 so that the few
-// tiles of a short call still occupy twice the CTA pairs, and 192 for
-// 256 < T <= 1024, where it fills the pairs' waves (a template parameter,
-// chosen from T alone).
+// tiles of a short call still occupy twice the CTA pairs; 192 where it fills
+// the pairs' waves better (at H = 7168, T in (256, 1024] and (1280, 1536]);
+// and 512 with a single shared partial from 4096 tokens on, when the wide
+// tiles need at most half the waves (a template parameter, chosen from T, P,
+// H and the SM count, never from the column range).
 //
 // Persistent, warp-specialized kernel, one CTA per SM, 7 warps per CTA:
 //   warp 0      operand producer: y [128 tokens x 64] and W [width/2 rows x 64]
@@ -34,8 +36,9 @@
 //   warps 2..5  epilogue, one token row per thread: sum the P partial boxes of
 //               a chunk in FP32 (p ascending), add the accumulator columns from
 //               this CTA's TMEM (two accumulators, so the next tile's MMAs run
-//               during this tile's epilogue), round to bf16 and store 16-byte
-//               vectors. When every pair owns a single tile there is no next
+//               during this tile's epilogue; one with 512-column tiles), round
+//               to bf16 and store 16-byte vectors. When every pair owns a
+//               single tile (and the tiles are not 512 wide) there is no next
 //               tile to overlap: the epilogue then parks each chunk's FP32 sums
 //               in the idle second accumulator's TMEM columns while the MMAs
 //               run, and adds them to the accumulator afterwards (same bits).
@@ -59,6 +62,17 @@ constexpr int kNarrowTileH = 128;  // T <= 256: twice the tiles, so twice the pa
 // waves (P = 8), so the launch takes it when (waves with 192) x 9 <= (waves
 // with 256) x 10: at H = 7168, T in (256, 1024] and (1280, 1536].
 constexpr int kMidTileH = 192;
+// 512-column tiles for a single shared partial (P = 1, where the tensor cores
+// bind): two N = 256 instructions per K-step into one 512-column accumulator.
+// Each CTA then takes in 48 KB per K-block for 128 x 512 outputs instead of
+// 32 KB for 128 x 256, at the price of the second accumulator: the epilogue
+// no longer overlaps the next tile's MMAs. Taken when the wide tiles need at
+// most half the waves of the 256-column ones (P = 1, H = 7168, projection us,
+// same box, 256 / 512 columns: T = 4096 90.4-90.6 / 87.4, T = 8192 173.9-176.3 /
+// 168.5-170.6; at T = 2048, 3 waves against 2 with the second one half empty,
+// 49.3 / 58.5). Below 4096 tokens they were not measured to win and are not used.
+constexpr int kWideTileH = 512;
+constexpr int kWideMinTokens = 4096;
 constexpr int kBlockK = 64;
 constexpr int kMaxStages = 6;
 constexpr int kChunk = 64;    // output columns per shared-partial box
@@ -98,6 +112,9 @@ constexpr int kMidStagesFewPartials = 5;
 constexpr int kMidSlotsFewPartials = 5;
 constexpr int kMidStagesManyPartials = 3;
 constexpr int kMidSlotsManyPartials = 8;
+// 512-column tiles: 48 KB stages, four of them beside the two slots of P = 1.
+constexpr int kWideStages = 4;
+constexpr int kWideSlots = 2;
 
 size_t smem_bytes(int stages, int slots, int tile_h) {
   return 1024 + static_cast<size_t>(stages) * stage_bytes_for(tile_h) +
@@ -140,6 +157,22 @@ __device__ __forceinline__ TileCoord tile_coord(const PrefillParams& p, int tile
   c.t0 = (tile / p.n_htiles) * (2 * kTileT) + rank * kTileT;
   c.h0 = (p.htile0 + tile % p.n_htiles) * kTileW;
   return c;
+}
+
+// First output column (relative to the tile's) of the 64 accumulator columns
+// [64 ch, 64 ch + 64). Each CTA of the pair holds tile_w / 2 consecutive W rows,
+// and an instruction takes the first half of its N columns from the even CTA's
+// rows and the second half from the odd CTA's. With 512-column tiles two N = 256
+// instructions per K-step take rows 0-127 and then 128-255 of each CTA, so the
+// accumulator's 128-column blocks hold tile columns 0, 256, 128 and 384.
+template <int kTileW>
+__device__ __forceinline__ int chunk_offset(int ch) {
+  if constexpr (kTileW > 256) {
+    const int blk = ch >> 1;
+    return ((blk & 1) << 8) | ((blk >> 1) << 7) | ((ch & 1) << 6);
+  } else {
+    return ch * kChunk;
+  }
 }
 
 // A 64-column chunk is processed only if it meets [col_start, col_end).
@@ -185,6 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
   const int n_stages = p.stages;
   constexpr int tile_h = kTileW;
+  constexpr bool kWide = kTileW > 256;   // two instructions per K-step, one accumulator
+  constexpr int kAccs = kWide ? 1 : 2;   // accumulators (each tile_h TMEM columns)
+  constexpr int kInstrN = kWide ? 256 : kTileW;
+  // Parking shared sums needs the idle second accumulator.
+  const bool stage_sums = !kWide && p.stage_sums != 0;
   constexpr int half_h = tile_h / 2;        // W rows loaded by each CTA of the pair
   constexpr int n_chunks = tile_h / kChunk;
   constexpr uint32_t stage_bytes = stage_bytes_for(tile_h);
@@ -277,12 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && my_tiles > 0) {
       if (rank == 0) {
         // ---------------- pair MMA issuer ----------------
-        const uint32_t idesc = umma_idesc_bf16(2 * kTileT, tile_h);
+        const uint32_t idesc = umma_idesc_bf16(2 * kTileT, kInstrN);
         int it = 0;
         bool alive = true;
         for (int i = 0; i < my_tiles && alive; ++i) {
-          const int acc = i & 1;
-          const uint32_t use = static_cast<uint32_t>(i >> 1);
+          const int acc = i % kAccs;
+          const uint32_t use = static_cast<uint32_t>(i / kAccs);
           if (!mbar_wait_cluster(smem_u32(&acce_bar[acc]), (use & 1u) ^ 1u, p.err, abort_v)) break;
           tc_fence_after();
           const uint32_t d = tmem + static_cast<uint32_t>(acc * tile_h);
@@ -297,9 +335,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t a = sbase + static_cast<uint32_t>(s) * stage_bytes;
             const uint32_t b = a + kAStage;
 #pragma unroll
-            for (int k = 0; k < kBlockK / 16; ++k)
+            for (int k = 0; k < kBlockK / 16; ++k) {
               umma_bf16_pair(d, umma_desc_sw128(a + 32u * k), umma_desc_sw128(b + 32u * k), idesc,
                              (kb | k) != 0 ? 1u : 0u);
+              if constexpr (kWide)  // W rows 128..255 of each CTA -> columns 256..511
+                umma_bf16_pair(d + 256u, umma_desc_sw128(a + 32u * k),
+                               umma_desc_sw128(b + 128u * 128u + 32u * k), idesc,
+                               (kb | k) != 0 ? 1u : 0u);
+            }
             umma_commit_pair(smem_u32(&empty_bar[s]), 0x3);
           }
           umma_commit_pair(smem_u32(&accf_bar[acc]), 0x3);
@@ -317,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileCoord c = tile_coord<kTileW>(p, pair + i * n_pairs, rank);
         if (c.t0 >= p.T) continue;  // no rows of this CTA in the tile
         for (int ch = 0; ch < n_chunks && alive; ++ch) {
-          const int hc = c.h0 + ch * kChunk;
+          const int hc = c.h0 + chunk_offset<kTileW>(ch);
           if (!chunk_active(p, hc)) continue;
           for (int pp = 0; pp < p.P; ++pp, ++k) {
             const int s = k % n_slots;
@@ -376,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int k = 0;
     bool alive = true;
     for (int i = 0; i < my_tiles && alive; ++i) {
-      const int acc = i & 1;
-      const uint32_t use = static_cast<uint32_t>(i >> 1);
+      const int acc = i % kAccs;
+      const uint32_t use = static_cast<uint32_t>(i / kAccs);
       const TileCoord c = tile_coord<kTileW>(p, pair + i * n_pairs, rank);
       const int t = c.t0 + r;
       const bool row_ok = t < p.T;
@@ -386,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool acc_ready = false;
 #pragma unroll 1
       for (int ch = 0; ch < n_chunks; ++ch) {
-        const int hc = c.h0 + ch * kChunk;
+        const int hc = c.h0 + chunk_offset<kTileW>(ch);
         const bool active = has_rows && chunk_active(p, hc);
         float s[kChunk];
 #pragma unroll
@@ -413,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!alive) break;
         }
-        if (p.stage_sums) {
+        if (stage_sums) {
           // Single tile per pair: the second accumulator's columns are idle, so
           // park this chunk's FP32 sums there and go on to the next chunk's
           // partials without waiting for the MMAs; the sums are added below.
@@ -441,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!active || !row_ok) continue;
         emit(t, hc, v0, v1, s);
       }
-      if (p.stage_sums && alive) {
+      if (stage_sums && alive) {
         // The parked sums plus the accumulator, chunk by chunk.
         tmem_wait_st();
         bool ok = mbar_wait_cluster(smem_u32(&accf_bar[acc]), use & 1u, p.err, abort_v);
@@ -453,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll 1
         for (int ch = 0; ch < n_chunks; ++ch) {
-          const int hc = c.h0 + ch * kChunk;
+          const int hc = c.h0 + chunk_offset<kTileW>(ch);
           const bool active = has_rows && chunk_active(p, hc);
           float v0[32], v1[32], sums[kChunk];
           __syncwarp();
@@ -476,8 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1 && rank == 0 && *abort_v && lane == 0) {
     const int last = my_tiles - 1;
-    for (int i = max(0, last - 1); i <= last; ++i)
-      wait_drain(smem_u32(&accf_bar[i & 1]), static_cast<uint32_t>(i >> 1) & 1u);
+    for (int i = max(0, last - (kAccs - 1)); i <= last; ++i)
+      wait_drain(smem_u32(&accf_bar[i % kAccs]), static_cast<uint32_t>(i / kAccs) & 1u);
   }
   __syncwarp();
   cluster_sync();
@@ -494,7 +537,8 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 cudaError_t setup_prefill(const DeviceInfo&) {
   for (const void* f : {reinterpret_cast<const void*>(prefill_kernel<kTileH>),
                         reinterpret_cast<const void*>(prefill_kernel<kMidTileH>),
-                        reinterpret_cast<const void*>(prefill_kernel<kNarrowTileH>)}) {
+                        reinterpret_cast<const void*>(prefill_kernel<kNarrowTileH>),
+                        reinterpret_cast<const void*>(prefill_kernel<kWideTileH>)}) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(kSmemLimit));
     if (e != cudaSuccess) return e;
@@ -520,13 +564,19 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
     const int groups = ceil_div(a.T, 2 * kTileT);
     const int pairs = std::max(1, dev.num_sms / 2);
     auto waves = [&](int w) { return ceil_div(groups * ceil_div(a.H, w), pairs); };
-    p.tile_h = 9 * waves(kMidTileH) <= 10 * waves(kTileH) ? kMidTileH : kTileH;
+    if (a.P == 1 && a.T >= kWideMinTokens && 2 * waves(kWideTileH) <= waves(kTileH))
+      p.tile_h = kWideTileH;
+    else
+      p.tile_h = 9 * waves(kMidTileH) <= 10 * waves(kTileH) ? kMidTileH : kTileH;
   }
   p.htile0 = a.col_start / p.tile_h;
   p.n_htiles = (a.col_end - 1) / p.tile_h - p.htile0 + 1;
   p.n_tpairs = ceil_div(a.T, 2 * kTileT);
   p.total_kb = ceil_div(a.L, kBlockK);
-  if (a.P == 1) {  // one box per chunk: the operand ring gets the bytes (measured)
+  if (p.tile_h == kWideTileH) {
+    p.stages = kWideStages;
+    p.slots = kWideSlots;
+  } else if (a.P == 1) {  // one box per chunk: the operand ring gets the bytes (measured)
     p.stages = kSinglePartialStages;
     p.slots = kSinglePartialSlots;
   } else if (p.tile_h == kNarrowTileH) {
@@ -550,7 +600,8 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
   p.pdl = a.pdl ? 1 : 0;
   p.err = dev.err_word;
   const long long tiles = static_cast<long long>(p.n_htiles) * p.n_tpairs;
-  p.stage_sums = tiles <= dev.num_sms / 2 ? 1 : 0;  // one tile per pair at most
+  // one tile per pair at most (and a second accumulator to park the sums in)
+  p.stage_sums = tiles <= dev.num_sms / 2 && p.tile_h != kWideTileH ? 1 : 0;
   const int grid = 2 * static_cast<int>(std::min<long long>(dev.num_sms / 2, tiles));
 
   // The shared partials as one 2-D tensor [P*T rows, H columns]: the box for
@@ -591,6 +642,8 @@ cudaError_t launch_prefill(const ProjectArgs& a, const DeviceInfo& dev, cudaStre
     return cudaLaunchKernelEx(&cfg, prefill_kernel<kNarrowTileH>, y_map, w_map, s_map, p);
   if (p.tile_h == kMidTileH)
     return cudaLaunchKernelEx(&cfg, prefill_kernel<kMidTileH>, y_map, w_map, s_map, p);
+  if (p.tile_h == kWideTileH)
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<kWideTileH>, y_map, w_map, s_map, p);
   return cudaLaunchKernelEx(&cfg, prefill_kernel<kTileH>, y_map, w_map, s_map, p);
 }
 

@@ -50,6 +50,7 @@ def test_overlapping_output_is_rejected():
     (3, 200, 512, 1024, 0, 1024), (3, 200, 512, 1024, 128, 896),   # decode above 128 tokens
     (3, 240, 512, 1024, 0, 1024), (3, 240, 512, 1024, 128, 896),   # prefill, 128-col tiles
     (8, 1000, 2048, 7168, 0, 7168),                                # production widths
+    (1, 4096, 256, 1544, 0, 1544), (1, 4096, 256, 1544, 136, 648),  # P = 1, 512-col tiles
 ])
 def test_in_place_into_a_shared_partial(P, T, L, H, c0, c1):
     """out aliasing shared[p] (the pages' in-place addmm_ into the shared output)

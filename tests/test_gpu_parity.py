@@ -132,6 +132,31 @@ def test_decode_tier_column_ranges_tile_the_full_call(T):
     assert torch.equal(pieces.view(torch.int16), full.view(torch.int16))
 
 
+@pytest.mark.parametrize("T,L,H", [
+    (4096, 2048, 7168),    # the first token count of the 512-column tiles, production widths
+    (4100, 328, 1416),     # ragged token group and K-block; the last tile ends inside its
+                           # fourth 128-column block (tile columns 384..391 of 512)
+    (4100, 64, 1032),      # one K-block; the last tile holds 8 columns, 4 tokens in the last group
+])
+def test_wide_tiles_single_partial(T, L, H):
+    """With one shared partial, T >= 4096 and at most half the waves of 256-column
+    tiles, the prefill kernel uses 512-column tiles
+    (two N = 256 instructions per K-step whose accumulator blocks hold tile columns
+    0, 256, 128, 384): every element against the oracle."""
+    check_full(inputs.make(1, T, L, H, seed=2600 + T), what=f"P1 T{T} L{L} H{H}")
+
+
+def test_wide_tiles_column_ranges_tile_the_full_call():
+    """Column ranges that cut 512-column tiles inside every 128-column block
+    reproduce the full call bit for bit, and write nothing outside their range."""
+    x = gh.to_dev(inputs.make(1, 4096, 256, 1544, seed=2700))
+    full = gh.run(x)
+    pieces = torch.full_like(full, float("nan"))
+    for c0, c1 in ((0, 136), (136, 648), (648, 1160), (1160, 1544)):
+        gh.run(x, c0, c1, out=pieces)
+    assert torch.equal(pieces.view(torch.int16), full.view(torch.int16))
+
+
 @pytest.mark.parametrize("T", [1, 2, 3])
 def test_one_launch_token_counts(T):
     """T <= 2 at the production widths (P = 8, L = 2048, H = 7168): the CUDA-core
