@@ -2,9 +2,10 @@
 
 Each case draws P, T, L, H and an aligned column range from a fixed seed, so
 the list is the same on every run. The token counts are spread over all the
-tiers (one-launch kernel, decode kernel with one, two or four K slices and the
-partials in or beside the stage ring, prefill kernel with 128-, 192- or
-256-column tiles), the widths over ragged multiples of 8. Every output element
+tiers (one-launch kernel, decode kernel with one, two, four or eight K slices
+and the partials in or beside the stage ring, prefill kernel with 128-, 192- or
+256-column tiles, and a few single-partial shapes on its 512-column tiles), the
+widths over ragged multiples of 8. Every output element
 inside the range must match the oracle within the bf16 tolerance, and every byte
 outside it must keep its sentinel value.
 """
@@ -44,12 +45,29 @@ def _cases(n=120, seed=2024):
     return cases
 
 
+def _wide_cases(n=8, seed=5):
+    """P = 1 shapes that select the 512-column prefill tiles (T >= 4096 and, at
+    H = 1032 ... 1536, half the waves of the 256-column tiles)."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        T = int(rng.choice([4096, 4100, 4200, 4352]))
+        H = 8 * int(rng.integers(129, 193))
+        L = 8 * int(rng.integers(1, 48))
+        c0 = 8 * int(rng.integers(0, H // 8))
+        c1 = 8 * int(rng.integers(c0 // 8 + 1, H // 8 + 1))
+        if rng.random() < 0.5:
+            c0, c1 = 0, H
+        cases.append((1, T, L, H, c0, c1, int(rng.integers(0, 2**31))))
+    return cases
+
+
 @pytest.fixture(scope="module", autouse=True)
 def lib():
     return gh.library()
 
 
-@pytest.mark.parametrize("P,T,L,H,c0,c1,seed", _cases())
+@pytest.mark.parametrize("P,T,L,H,c0,c1,seed", _cases() + _wide_cases())
 def test_random_shape_matches_oracle(P, T, L, H, c0, c1, seed):
     x = gh.to_dev(inputs.make(P, T, L, H, seed=seed))
     out = torch.full((T, H), SENTINEL, dtype=torch.int16, device="cuda").view(torch.bfloat16)
